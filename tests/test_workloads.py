@@ -1,0 +1,35 @@
+"""The seeded input generators: determinism, shapes and positive definiteness."""
+
+import numpy as np
+import pytest
+
+from workloads import make_config, random_problem, row_absmax_scales
+
+
+def test_c1_c2_deterministic_and_shaped():
+    for key, (m, n, bits) in {"c1": (64, 64, 0), "c2": (1024, 1024, 4)}.items():
+        p1, p2 = make_config(key), make_config(key)
+        assert p1.digest() == p2.digest()
+        assert (p1.m, p1.n, p1.bits) == (m, n, bits)
+        assert p1.W.shape == (m, n) and p1.A.shape == (n, n) and p1.B.shape == (m, m)
+        for M in (p1.A, p1.B):
+            assert M.dtype == np.float32 and np.array_equal(M, M.T)
+            assert np.linalg.eigvalsh(M.astype(np.float64)).min() > 0
+        if bits:
+            assert p1.scales.shape == (m,) and np.all(p1.scales > 0)
+        else:
+            assert p1.scales is None
+
+
+def test_absmax_scale_rule():
+    W = np.array([[0.7, -1.4, 0.0], [0.3, 0.1, -0.2]], dtype=np.float32)
+    assert np.allclose(row_absmax_scales(W, 4), [1.4 / 7, 0.3 / 7])
+    assert np.allclose(row_absmax_scales(W, 2), [1.4, 0.3])
+
+
+@pytest.mark.parametrize("kind", ["gram", "identity_b", "diagonal", "ar1"])
+def test_random_problem_kinds(kind):
+    p = random_problem(7, 5, bits=3, seed=1, kind=kind)
+    assert p.W.shape == (7, 5) and p.A.shape == (5, 5) and p.B.shape == (7, 7)
+    assert np.linalg.eigvalsh(p.A.astype(np.float64)).min() > 0
+    assert np.linalg.eigvalsh(p.B.astype(np.float64)).min() > 0
