@@ -1,0 +1,154 @@
+/*
+ * bakron.h -- C ABI of libbakron.so, a GB300 (sm_103a) implementation of the
+ * BaKron solver: two-sided adaptive rounding of a weight matrix under a
+ * Kronecker-factored Hessian A (x) B.
+ *
+ * Source: "BaKron: Efficient Quantization with Kronecker-Factored Hessians"
+ * (arXiv 2608.06291).
+ *
+ * Conventions for every entry point
+ *   - Matrices are dense, row-major, 32-bit float unless stated otherwise.
+ *   - W is m x n (m outputs = rows, n inputs = columns).  A (n x n) is the
+ *     input-side factor and B (m x m) the output-side factor of the Hessian
+ *     A (x) B of vec(W) (Sec. 3.1, Proposition 3.1: (A (x) B) vec(W) =
+ *     vec(B W A^T), vec column-major).
+ *   - "device" pointers must be CUDA device memory of the current device;
+ *     "host" pointers are ordinary (preferably pinned) host memory.
+ *   - The caller owns every buffer, including the workspace; the library
+ *     allocates no memory in these calls.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and runs asynchronously, except where a
+ *     function says it synchronizes.
+ *   - Argument errors are returned synchronously before anything is
+ *     enqueued.  Conditions only the device can see (a non-positive pivot,
+ *     a non-finite input) are written to a caller-provided device status
+ *     word; nothing traps or asserts on the device.
+ *   - Return values are bakron_status codes.
+ */
+#ifndef BAKRON_H_
+#define BAKRON_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BAKRON_ABI_VERSION 1
+
+typedef enum bakron_status {
+  BAKRON_OK = 0,
+  BAKRON_ERR_INVALID_ARG = 1, /* bad size, bit width, null pointer, aliasing */
+  BAKRON_ERR_NOT_SPD = 2,     /* reserved: a factor reported a non-positive pivot */
+  BAKRON_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy) */
+  BAKRON_ERR_WORKSPACE = 4,   /* workspace null, misaligned or smaller than required */
+  BAKRON_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
+} bakron_status;
+
+/* Device status-word bits written by bakron_quantize (0 = success). */
+#define BAKRON_DEV_NONFINITE_W 1 /* W holds a NaN or an infinity */
+#define BAKRON_DEV_BAD_SCALE 2   /* a scale is <= 0, NaN or infinite */
+#define BAKRON_DEV_TIMEOUT 4     /* a bounded device-side wait gave up */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* bakron_status_string(int status);
+
+/* BAKRON_ABI_VERSION of the loaded library. */
+int bakron_abi_version(void);
+
+/* ---------------------------------------------------------------- prepare
+ * Factor preparation, Sec. 3.2 Algorithm 1 prologue (also Algorithms 2, 3,
+ * 5, 6; App. B: done once, at the top level):
+ *     L = Cholesky(H^-1), then every column divided by its diagonal entry,
+ * giving the unit lower-triangular L-hat.  Computed without forming H^-1:
+ * with H = U D U^T (U unit upper triangular, factored from the last index
+ * backwards), L-hat = U^-T.  Arithmetic is double-float (pairs of fp32,
+ * about 44 significant bits); the result is rounded once to fp32.
+ */
+
+/* Workspace bytes bakron_factor needs for a factor of order d (d >= 1). */
+size_t bakron_factor_workspace_size(int64_t d);
+
+/* H: device, d x d, symmetric positive definite (the caller adds any
+ *    damping); only the lower triangle is read.
+ * Lhat: device, d x d, written in full: unit lower triangular, zeros above
+ *    the diagonal.  May not alias H.
+ * ws: device, >= bakron_factor_workspace_size(d) bytes, 256-byte aligned.
+ * info_dev: device int32; set to 0 on success, or to 1 + the index of the
+ *    first non-positive pivot met (the factorization runs from the last
+ *    index backwards; Lhat is then undefined).
+ */
+int bakron_factor(const float* H, int64_t d, float* Lhat, void* ws, size_t ws_bytes,
+                  int32_t* info_dev, void* stream);
+
+/* Workspace bytes bakron_prepare needs (max over the two factors). */
+size_t bakron_prepare_workspace_size(int64_t m, int64_t n);
+
+/* Both factors: LA = L-hat of A (n x n), LB = L-hat of B (m x m).
+ * A, B, LA, LB, ws: device.  info_dev: device int32[2], info for A then B,
+ * as in bakron_factor.  The two factorizations run one after the other on
+ * `stream` and share `ws`.
+ */
+int bakron_prepare(const float* A, const float* B, int64_t m, int64_t n, float* LA, float* LB,
+                   void* ws, size_t ws_bytes, int32_t* info_dev, void* stream);
+
+/* ---------------------------------------------------------------- quantize
+ * The BaKron core, Sec. 3.5 Algorithm 6 (equal to Algorithms 2, 3, 5 by
+ * Theorem 3.2): with anti-diagonals processed in order and
+ *     W~ = W0 + L_B E_(earlier) L_A^T (App. B eq. (2)),
+ *     v_ij = clamp(round_half_even(fp32(W~_ij) / s_i), lo, hi),
+ *     E_ij = s_i v_ij - W~_ij,
+ * executed as a tile wavefront: tiles on one tile anti-diagonal are solved
+ * in parallel (Sec. 3.3), and the errors of a finished tile are pushed to
+ * later tiles as dense products (Sec. 3.4/3.5, App. B eq. (1)).
+ * All accumulation is double-float: values are unevaluated sums of two fp32
+ * numbers (about 44 significant bits), products are summed with an
+ * error-free offset accumulator (Rump, Ogita and Oishi, "Accurate
+ * floating-point summation, part I", 2008, ExtractScalar).
+ */
+
+/* Workspace bytes bakron_quantize needs for an m x n problem. */
+size_t bakron_quantize_workspace_size(int64_t m, int64_t n);
+
+/* W: device, m x n; read only.
+ * LA: device, n x n unit lower-triangular L-hat of A (entries above the
+ *     diagonal are ignored; the diagonal is taken as 1).
+ * LB: device, m x m unit lower-triangular L-hat of B (same).
+ * scales: device, m per-row scales (> 0, finite), or NULL for all ones.
+ * bits: 0 for the unbounded alphabet Z (plain rounding), or 2..8 for the
+ *     alphabet {-2^(bits-1) .. 2^(bits-1) - 1} (Sec. 3.1).
+ * V: device int32, m x n: the integer codes.
+ * Wq: device, m x n: fp32(scales[i] * V[i][j]).  W, V and Wq must be
+ *     three distinct buffers.
+ * ws: device, >= bakron_quantize_workspace_size(m, n) bytes, 256-byte
+ *     aligned; its contents on entry do not matter.
+ * status_dev: device int32; set to 0, or to an OR of BAKRON_DEV_* bits.
+ *     With BAKRON_DEV_NONFINITE_W or BAKRON_DEV_BAD_SCALE set, V and Wq
+ *     are undefined.
+ * m, n >= 1 and m * n < 2^31.
+ */
+int bakron_quantize(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                    int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                    int32_t* status_dev, void* stream);
+
+/* Device workspace bytes bakron_quantize_host needs: the device copies of
+ * W, LA, LB, scales, V, Wq and the status word, plus
+ * bakron_quantize_workspace_size(m, n). */
+size_t bakron_quantize_host_workspace_size(int64_t m, int64_t n);
+
+/* Same computation from and to HOST buffers: copies W, LA, LB, scales into
+ * `dev_ws`, runs bakron_quantize, copies V and Wq back, and synchronizes
+ * `stream` before returning.  scales may be NULL.  *status_host receives
+ * the device status word.  dev_ws: device, >= bakron_quantize_host_
+ * workspace_size(m, n) bytes, 256-byte aligned.
+ */
+int bakron_quantize_host(const float* W, const float* LA, const float* LB, const float* scales,
+                         int bits, int64_t m, int64_t n, int32_t* V, float* Wq, void* dev_ws,
+                         size_t dev_ws_bytes, int32_t* status_host, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BAKRON_H_ */

@@ -1,0 +1,158 @@
+"""BaKron on GB300: Python binding of libbakron.so.
+
+Thin argument marshalling over the C ABI declared in include/bakron.h: torch
+is used only to allocate device memory and to name the current stream; every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+fallback: if the library is missing, every call raises.
+
+Source of the method: "BaKron: Efficient Quantization with Kronecker-Factored
+Hessians" (arXiv 2608.06291), Sec. 3.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+from . import _lib
+
+__all__ = [
+    "load_library",
+    "factor",
+    "prepare",
+    "quantize",
+    "quantize_host",
+    "quantize_workspace_size",
+    "prepare_workspace_size",
+]
+
+
+def load_library():
+    return _lib.load()
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_handle(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _require_cuda_f32(t, shape, name):
+    torch = _torch()
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == tuple(shape)):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {tuple(shape)}")
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    # torch's caching allocator hands out blocks aligned to at least 256 bytes
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def prepare_workspace_size(m: int, n: int) -> int:
+    return int(_lib.load().bakron_prepare_workspace_size(m, n))
+
+
+def quantize_workspace_size(m: int, n: int) -> int:
+    return int(_lib.load().bakron_quantize_workspace_size(m, n))
+
+
+def factor(H, ws=None, stream=None):
+    """L-hat = Cholesky(H^-1) with unit-normalized columns (fp32, d x d).
+
+    Returns (Lhat, info) where info is a 1-element int32 CUDA tensor: 0, or
+    1 + the index of the first non-positive pivot met.
+    """
+    torch = _torch()
+    lib = _lib.load()
+    d = H.shape[0]
+    _require_cuda_f32(H, (d, d), "H")
+    L = torch.empty_like(H)
+    info = torch.zeros(1, dtype=torch.int32, device=H.device)
+    if ws is None:
+        ws = _workspace(lib.bakron_factor_workspace_size(d), H.device)
+    st = lib.bakron_factor(_ptr(H), d, _ptr(L), _ptr(ws), ws.numel(), _ptr(info), _stream_handle(stream))
+    _lib.check(st, "bakron_factor")
+    return L, info
+
+
+def prepare(A, B, ws=None, stream=None):
+    """(L-hat_A, L-hat_B, info[2]) for the input-side A (n x n) and output-side B (m x m)."""
+    torch = _torch()
+    lib = _lib.load()
+    n, m = A.shape[0], B.shape[0]
+    _require_cuda_f32(A, (n, n), "A")
+    _require_cuda_f32(B, (m, m), "B")
+    LA = torch.empty_like(A)
+    LB = torch.empty_like(B)
+    info = torch.zeros(2, dtype=torch.int32, device=A.device)
+    if ws is None:
+        ws = _workspace(lib.bakron_prepare_workspace_size(m, n), A.device)
+    st = lib.bakron_prepare(_ptr(A), _ptr(B), m, n, _ptr(LA), _ptr(LB), _ptr(ws), ws.numel(), _ptr(info),
+                            _stream_handle(stream))
+    _lib.check(st, "bakron_prepare")
+    return LA, LB, info
+
+
+def quantize(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=None):
+    """BaKron quantization of W (m x n) given the normalized factors.
+
+    Returns (V int32, Wq float32, status int32[1]) -- all CUDA tensors; the
+    status word is 0 on success (BAKRON_DEV_* bits otherwise).
+    """
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    _require_cuda_f32(LA, (n, n), "LA")
+    _require_cuda_f32(LB, (m, m), "LB")
+    if scales is not None:
+        _require_cuda_f32(scales, (m,), "scales")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, device=W.device)
+        Wq = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    else:
+        V, Wq, status = out
+    if ws is None:
+        ws = _workspace(lib.bakron_quantize_workspace_size(m, n), W.device)
+    st = lib.bakron_quantize(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
+                             _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
+    _lib.check(st, "bakron_quantize")
+    return V, Wq, status
+
+
+def quantize_host(W, LA, LB, scales=None, bits: int = 0, dev_ws=None, out=None, stream=None) -> Tuple:
+    """Same as quantize() from and to HOST (CPU, ideally pinned) torch tensors.
+
+    The library copies the inputs to the device workspace, solves, copies V
+    and Wq back and synchronizes.  Returns (V, Wq, status:int).
+    """
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    for t, shp, name in ((W, (m, n), "W"), (LA, (n, n), "LA"), (LB, (m, m), "LB")):
+        if t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be a contiguous float32 CPU tensor of shape {shp}")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, pin_memory=True)
+        Wq = torch.empty((m, n), dtype=torch.float32, pin_memory=True)
+    else:
+        V, Wq = out
+    if dev_ws is None:
+        dev_ws = _workspace(lib.bakron_quantize_host_workspace_size(m, n), torch.device("cuda"))
+    status = ctypes.c_int32(0)
+    st = lib.bakron_quantize_host(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
+                                  _ptr(dev_ws), dev_ws.numel(), ctypes.addressof(status), _stream_handle(stream))
+    _lib.check(st, "bakron_quantize_host")
+    return V, Wq, int(status.value)

@@ -1,0 +1,140 @@
+// abi.cu -- the extern "C" entry points of libbakron.so (declared in bakron.h).
+//
+// Every entry point validates its arguments on the host and returns a
+// bakron_status before enqueuing anything; device-side conditions go to the
+// caller's device status words.
+#include <cstdint>
+
+#include "bakron.h"
+#include "internal.h"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? BAKRON_OK : BAKRON_ERR_CUDA; }
+
+constexpr int64_t kMaxElems = (int64_t)1 << 31;  // m * n and d * d limit (int indexing)
+
+}  // namespace
+
+extern "C" {
+
+const char* bakron_status_string(int status) {
+  switch (status) {
+    case BAKRON_OK: return "BAKRON_OK";
+    case BAKRON_ERR_INVALID_ARG: return "BAKRON_ERR_INVALID_ARG";
+    case BAKRON_ERR_NOT_SPD: return "BAKRON_ERR_NOT_SPD";
+    case BAKRON_ERR_CUDA: return "BAKRON_ERR_CUDA";
+    case BAKRON_ERR_WORKSPACE: return "BAKRON_ERR_WORKSPACE";
+    case BAKRON_ERR_TIMEOUT: return "BAKRON_ERR_TIMEOUT";
+    default: return "BAKRON_ERR_UNKNOWN";
+  }
+}
+
+int bakron_abi_version(void) { return BAKRON_ABI_VERSION; }
+
+size_t bakron_factor_workspace_size(int64_t d) {
+  if (d < 1 || d * d >= kMaxElems) return 0;
+  return bakron::factor_workspace_bytes(d);
+}
+
+int bakron_factor(const float* H, int64_t d, float* Lhat, void* ws, size_t ws_bytes, int32_t* info_dev,
+                  void* stream) {
+  if (!H || !Lhat || !info_dev || d < 1 || d * d >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)H == (const void*)Lhat) return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::factor_workspace_bytes(d))
+    return BAKRON_ERR_WORKSPACE;
+  return from_cuda(bakron::factor_launch(H, (int)d, Lhat, ws, info_dev, (cudaStream_t)stream));
+}
+
+size_t bakron_prepare_workspace_size(int64_t m, int64_t n) {
+  const size_t a = bakron_factor_workspace_size(n), b = bakron_factor_workspace_size(m);
+  if (a == 0 || b == 0) return 0;
+  return a > b ? a : b;
+}
+
+int bakron_prepare(const float* A, const float* B, int64_t m, int64_t n, float* LA, float* LB, void* ws,
+                   size_t ws_bytes, int32_t* info_dev, void* stream) {
+  if (!A || !B || !LA || !LB || !info_dev || m < 1 || n < 1) return BAKRON_ERR_INVALID_ARG;
+  if (m * m >= kMaxElems || n * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)A == (const void*)LA || (const void*)B == (const void*)LB || LA == LB)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron_prepare_workspace_size(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = bakron::factor_launch(A, (int)n, LA, ws, info_dev, s);
+  if (e != cudaSuccess) return BAKRON_ERR_CUDA;
+  return from_cuda(bakron::factor_launch(B, (int)m, LB, ws, info_dev + 1, s));
+}
+
+size_t bakron_quantize_workspace_size(int64_t m, int64_t n) {
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return 0;
+  return bakron::quantize_workspace_bytes(m, n);
+}
+
+int bakron_quantize(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                    int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                    int32_t* status_dev, void* stream) {
+  if (!W || !LA || !LB || !V || !Wq || !status_dev) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if (!(bits == 0 || (bits >= 2 && bits <= 8))) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)Wq == (const void*)W || (const void*)V == (const void*)W || (void*)V == (void*)Wq)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  return from_cuda(bakron::quantize_launch(W, LA, LB, scales, bits, (int)m, (int)n, V, Wq, ws, status_dev,
+                                           (cudaStream_t)stream));
+}
+
+size_t bakron_quantize_host_workspace_size(int64_t m, int64_t n) {
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return 0;
+  using bakron::align_up;
+  const size_t mn = (size_t)m * (size_t)n;
+  return align_up(mn * 4) * 3 + align_up((size_t)n * n * 4) + align_up((size_t)m * m * 4) +
+         align_up((size_t)m * 4) + align_up(4) + bakron::quantize_workspace_bytes(m, n);
+}
+
+int bakron_quantize_host(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                         int64_t m, int64_t n, int32_t* V, float* Wq, void* dev_ws, size_t dev_ws_bytes,
+                         int32_t* status_host, void* stream) {
+  if (!W || !LA || !LB || !V || !Wq || !status_host) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if (!(bits == 0 || (bits >= 2 && bits <= 8))) return BAKRON_ERR_INVALID_ARG;
+  if (!dev_ws || !aligned(dev_ws, bakron::kAlign) || dev_ws_bytes < bakron_quantize_host_workspace_size(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  using bakron::align_up;
+  const size_t mn = (size_t)m * (size_t)n;
+  char* p = static_cast<char*>(dev_ws);
+  float* dW = reinterpret_cast<float*>(p);
+  p += align_up(mn * 4);
+  int32_t* dV = reinterpret_cast<int32_t*>(p);
+  p += align_up(mn * 4);
+  float* dWq = reinterpret_cast<float*>(p);
+  p += align_up(mn * 4);
+  float* dLA = reinterpret_cast<float*>(p);
+  p += align_up((size_t)n * n * 4);
+  float* dLB = reinterpret_cast<float*>(p);
+  p += align_up((size_t)m * m * 4);
+  float* dS = reinterpret_cast<float*>(p);
+  p += align_up((size_t)m * 4);
+  int32_t* dStatus = reinterpret_cast<int32_t*>(p);
+  p += align_up(4);
+  void* qws = p;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(dW, W, mn * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dLA, LA, (size_t)n * n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dLB, LB, (size_t)m * m * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && scales) e = cudaMemcpyAsync(dS, scales, (size_t)m * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return BAKRON_ERR_CUDA;
+  e = bakron::quantize_launch(dW, dLA, dLB, scales ? dS : nullptr, bits, (int)m, (int)n, dV, dWq, qws, dStatus,
+                              s);
+  if (e != cudaSuccess) return BAKRON_ERR_CUDA;
+  e = cudaMemcpyAsync(V, dV, mn * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(Wq, dWq, mn * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(status_host, dStatus, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return from_cuda(e);
+}
+
+}  // extern "C"

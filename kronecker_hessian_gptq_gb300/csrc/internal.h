@@ -1,0 +1,25 @@
+// internal.h -- declarations shared by the translation units of libbakron.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bakron {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// quantize.cu
+size_t quantize_workspace_bytes(int64_t m, int64_t n);
+cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
+                            int bits, int m, int n, int32_t* V, float* Wq, void* ws,
+                            int32_t* status_dev, cudaStream_t stream);
+
+// prep.cu
+size_t factor_workspace_bytes(int64_t d);
+cudaError_t factor_launch(const float* H, int d, float* Lhat, void* ws, int32_t* info_dev,
+                          cudaStream_t stream);
+
+}  // namespace bakron

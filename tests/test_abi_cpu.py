@@ -1,0 +1,104 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host -- no GPU needed (no compute call is made)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "bakron.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import kronecker_hessian_gptq_gb300 as bk
+    from kronecker_hessian_gptq_gb300 import build as b
+
+    b.build()
+    return bk.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bakron_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for need in ("bakron_prepare", "bakron_quantize", "bakron_factor", "bakron_quantize_host",
+                 "bakron_status_string", "bakron_abi_version"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from kronecker_hessian_gptq_gb300 import _lib
+
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.bakron_abi_version() == 1
+    assert lib.bakron_status_string(0) == b"BAKRON_OK"
+    assert lib.bakron_status_string(4) == b"BAKRON_ERR_WORKSPACE"
+    assert lib.bakron_status_string(99) == b"BAKRON_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    assert lib.bakron_quantize_workspace_size(0, 5) == 0
+    assert lib.bakron_quantize_workspace_size(64, 64) >= 3 * 64 * 64 * 8
+    q = lib.bakron_quantize_workspace_size(100, 37)
+    assert lib.bakron_quantize_host_workspace_size(100, 37) > q
+    assert lib.bakron_factor_workspace_size(0) == 0
+    assert lib.bakron_prepare_workspace_size(10, 20) == max(
+        lib.bakron_factor_workspace_size(10), lib.bakron_factor_workspace_size(20))
+
+
+def test_quantize_rejects_bad_arguments_before_any_launch(lib):
+    W = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    V, Wq = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    ws = ctypes.c_void_p(0x100000)
+    big = lib.bakron_quantize_workspace_size(8, 8)
+    q = lib.bakron_quantize
+    assert q(W, W, W, None, 4, 0, 8, V, Wq, ws, big, W, None) == 1  # m < 1
+    assert q(W, W, W, None, 4, 8, 0, V, Wq, ws, big, W, None) == 1  # n < 1
+    for bits in (1, 9, -1, 16):
+        assert q(W, W, W, None, bits, 8, 8, V, Wq, ws, big, W, None) == 1
+    assert q(None, W, W, None, 4, 8, 8, V, Wq, ws, big, W, None) == 1  # null W
+    assert q(W, W, W, None, 4, 8, 8, V, Wq, ws, big, None, None) == 1  # null status
+    assert q(W, W, W, None, 4, 8, 8, V, W, ws, big, W, None) == 1  # Wq aliases W
+    assert q(W, W, W, None, 4, 8, 8, V, V, ws, big, W, None) == 1  # Wq aliases V
+    assert q(W, W, W, None, 4, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
+    assert q(W, W, W, None, 4, 8, 8, V, Wq, None, big, W, None) == 4  # null workspace
+    assert q(W, W, W, None, 4, 8, 8, V, Wq, ctypes.c_void_p(0x100010), big, W, None) == 4  # misaligned
+    assert q(W, W, W, None, 4, 1 << 16, 1 << 16, V, Wq, ws, big, W, None) == 1  # m*n too large
+
+
+def test_prepare_and_factor_reject_bad_arguments(lib):
+    H = ctypes.c_void_p(0x1000)
+    L = ctypes.c_void_p(0x2000)
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.bakron_factor(H, 0, L, ws, 1 << 30, H, None) == 1
+    assert lib.bakron_factor(H, 8, H, ws, 1 << 30, H, None) == 1  # H aliases Lhat
+    assert lib.bakron_factor(H, 8, L, ws, 16, H, None) == 4
+    assert lib.bakron_prepare(H, ctypes.c_void_p(0x1100), 0, 4, L, ctypes.c_void_p(0x3000), ws, 1 << 30, H,
+                              None) == 1
+    assert lib.bakron_prepare(H, ctypes.c_void_p(0x1100), 4, 4, L, L, ws, 1 << 30, H, None) == 1  # LA is LB
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    from kronecker_hessian_gptq_gb300 import _lib
+
+    saved = _lib._lib
+    try:
+        _lib._lib = None
+        with pytest.raises(RuntimeError, match="libbakron.so not found"):
+            _lib.load(str(tmp_path / "missing.so"))
+    finally:
+        _lib._lib = saved
