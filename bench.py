@@ -1,0 +1,342 @@
+"""Benchmark of the BaKron solve (bakron_quantize) on one m x n layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3] [--impl ours|reference]
+
+One step = one bakron_quantize call over the whole layer (every anti-
+diagonal, every propagation), inputs resident in HBM; the factor preparation
+is timed once and reported separately, as the paper's Table 3 excludes it.
+Default workload: c3, the 4096 x 4096 attention-projection shape with an
+AR(1) output factor and a 4-bit alphabet (see workloads/configs.py).
+
+Multi-GPU: one layer per GPU, no communication (independent replicas):
+`value` = N * m * n / max over ranks of the timed time.  L2 is flushed
+(a 512 MiB write) before every timed step, outside the step's events.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload: the first R rows of the layer (their codes do
+not depend on later rows), so the unit stays weights/s.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "BaKron solve time & weights quantized/s per m×n layer; % of tensor roofline"
+UNIT = "weights/s"
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+# One double-float multiply-add (2 algorithmic flops) costs 5 fp32 pipe
+# instructions (offset accumulator, df.cuh).
+DF_INSTR_PER_MAC = 5
+
+
+def alu_peak_tflops(sm_max_mhz: float) -> float:
+    """Algorithmic TFLOP/s of the fp32 pipes running double-float MACs."""
+    lane_ops = SM_COUNT * FP32_LANES_PER_SM * sm_max_mhz * 1e6
+    return 2.0 * lane_ops / DF_INSTR_PER_MAC / 1e12
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def aggregate_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world <= 1:
+        return
+    import torch.distributed as dist
+
+    if device is not None and device.type == "cuda":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def load_workload(key: str):
+    from workloads import make_config
+
+    return make_config(key)
+
+
+def workload_config(p, world: int) -> dict:
+    alpha = "Z" if p.bits == 0 else "{%d..%d}" % (-(1 << (p.bits - 1)), (1 << (p.bits - 1)) - 1)
+    return {"workload": p.name, "m": p.m, "n": p.n, "bits": p.bits, "alphabet": alpha,
+            "scales": "per-row absmax" if p.scales is not None else "none",
+            "global_batch": world, "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "flushed by a 512 MiB write before every timed step", "inputs": p.digest()}
+
+
+def oracle_sample(p, rows: int, LA64, LB64):
+    """The oracle on the first `rows` rows (codes of a row depend only on rows above it)."""
+    import oracle as O
+
+    r = min(rows, p.m)
+    s = None if p.scales is None else p.scales[:r]
+    t0 = time.perf_counter()
+    O.bakron(p.W[:r], LA=LA64, LB=LB64[:r, :r], scales=s, bits=p.bits)
+    return r * p.n, time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, on a bounded sample per step."""
+    if rank != 0:
+        return None
+    import oracle as O
+
+    p = load_workload(args.config)
+    LA64, LB64 = O.factors_of(p.A, p.B)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(p, rows, LA64, LB64)
+    times, units = [], 0
+    for _ in range(args.steps):
+        u, t = oracle_sample(p, rows, LA64, LB64)
+        times.append(t)
+        units = u
+    tot = sum(times)
+    value = units * args.steps / tot
+    sample = f"first {min(rows, p.m)} of {p.m} rows x {p.n} columns per step (fp64 numpy, Alg. 5 recursion)"
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(p, 1), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def run_ours(args, rank, local_rank, world):
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import kronecker_hessian_gptq_gb300 as bk
+    from kronecker_hessian_gptq_gb300 import _lib
+
+    lib = bk.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    p = load_workload(args.config)
+    m, n = p.m, p.n
+    A, B, W = (torch.from_numpy(x).to(dev) for x in (p.A, p.B, p.W))
+    s = None if p.scales is None else torch.from_numpy(p.scales).to(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record()
+    LA, LB, info = bk.prepare(A, B)
+    e1.record()
+    torch.cuda.synchronize()
+    prep_ms = e0.elapsed_time(e1)
+    if info.abs().sum().item() != 0:
+        raise RuntimeError(f"factor preparation reported a non-positive pivot: {info.tolist()}")
+
+    ws = torch.empty(bk.quantize_workspace_size(m, n), dtype=torch.uint8, device=dev)
+    out = (torch.empty((m, n), dtype=torch.int32, device=dev), torch.empty((m, n), dtype=torch.float32, device=dev),
+           torch.zeros(1, dtype=torch.int32, device=dev))
+    flush = torch.empty((512 << 20) // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    starts, ends = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record()
+        bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)
+        ends[k].record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if out[2].item() != 0:
+        raise RuntimeError(f"device status {out[2].item()}")
+    total_ms = aggregate_max(sum(step_ms), world, dev)
+
+    # Per-kernel timing pass (events around every launch), after the timed region.
+    kms = (ctypes.c_double * 3)()
+    kl = (ctypes.c_int64 * 3)()
+    kf = (ctypes.c_double * 3)()
+    for _ in range(2):
+        flush.zero_()
+        st = lib.bakron_quantize_profile(W.data_ptr(), LA.data_ptr(), LB.data_ptr(), None if s is None else s.data_ptr(),
+                                         p.bits, m, n, out[0].data_ptr(), out[1].data_ptr(), ws.data_ptr(), ws.numel(),
+                                         out[2].data_ptr(), torch.cuda.current_stream().cuda_stream, kms, kl, kf)
+        _lib.check(st, "bakron_quantize_profile")
+    kernels = {name: {"ms": kms[c], "launches": kl[c], "alg_tflops": (kf[c] / (kms[c] * 1e-3) / 1e12) if kms[c] else 0}
+               for c, name in enumerate(_lib.KERNEL_CLASSES)}
+    dom = max(range(3), key=lambda c: kms[c])
+    launches_per_step = 2 * kl[0] + kl[1] + kl[2]
+
+    # End to end through the host entry point: pinned host inputs in, codes out.
+    Wh = torch.from_numpy(p.W).pin_memory()
+    LAh, LBh = LA.cpu().pin_memory(), LB.cpu().pin_memory()
+    sh = None if p.scales is None else torch.from_numpy(p.scales).pin_memory()
+    hout = (torch.empty((m, n), dtype=torch.int32, pin_memory=True),
+            torch.empty((m, n), dtype=torch.float32, pin_memory=True))
+    dws = torch.empty(lib.bakron_quantize_host_workspace_size(m, n), dtype=torch.uint8, device=dev)
+    bk.quantize_host(Wh, LAh, LBh, sh, p.bits, dev_ws=dws, out=hout)
+    barrier(world, dev)
+    e2e = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        bk.quantize_host(Wh, LAh, LBh, sh, p.bits, dev_ws=dws, out=hout)
+        e2e.append(time.perf_counter() - t0)
+    e2e_s = aggregate_max(sum(e2e), world, dev)
+    if not np.array_equal(hout[0].numpy(), out[0].cpu().numpy()):
+        raise RuntimeError("host entry point disagrees with the device entry point")
+
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = alu_peak_tflops(sm_max)
+    achieved = kf[dom] / kl[dom] / (kms[dom] / kl[dom] * 1e-3) / 1e12
+    f_alg = float(m) * n * (m + n)
+    res = {
+        "metric": METRIC, "value": world * m * n * args.steps / (total_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32x2 double-float", "data": "synthetic",
+        "config": workload_config(p, world),
+        "solve_alg_tflops": f_alg / (total_ms / args.steps * 1e-3) / 1e12,
+        "prep_ms": prep_ms,
+        "roofline": {"bound": "alu", "kernel": _lib.KERNEL_CLASSES[dom], "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_max:.0f} MHz / "
+                                   f"{DF_INSTR_PER_MAC} instr per double-float MAC x 2 flops"},
+        "kernels": kernels,
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+        "e2e": {"value": world * m * n * args.steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": 4 * (m * n + n * n + m * m + (m if p.scales is not None else 0)),
+                "d2h_bytes_per_step": 8 * m * n + 4},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as O
+
+        LA64, LB64 = O.factors_of(p.A, p.B)
+        units, secs = oracle_sample(p, args.cpu_rows, LA64, LB64)
+        res["cpu_baseline"] = {"value": units / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                               "sample": f"first {min(args.cpu_rows, m)} of {m} rows x {n} columns, one solve "
+                                         f"({secs:.1f} s, fp64 numpy, Alg. 5 recursion)"}
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c3")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            world = 1
+        else:
+            import torch
+
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+    res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, local_rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

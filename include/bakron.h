@@ -132,6 +132,22 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
                     int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                     int32_t* status_dev, void* stream);
 
+/* Diagnostics: bakron_quantize with CUDA events recorded around every
+ * kernel launch, for per-kernel timing.  Same arguments and result as
+ * bakron_quantize, plus three arrays of BAKRON_KERNEL_CLASSES entries
+ * (host memory) receiving, per kernel class, the summed event time in ms,
+ * the number of launches and the algorithmic flops (2 per multiply-add of
+ * the products L_B E L_A^T the class computes).  Classes: 0 = input
+ * check and state set-up, 1 = tile solve (diagonal blocks), 2 = forward
+ * propagation (off-diagonal blocks).  Synchronizes `stream` before it
+ * returns; the events add a little time to every launch.
+ */
+#define BAKRON_KERNEL_CLASSES 3
+int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                            int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                            int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,
+                            double* kernel_flops);
+
 /* Device workspace bytes bakron_quantize_host needs: the device copies of
  * W, LA, LB, scales, V, Wq and the status word, plus
  * bakron_quantize_workspace_size(m, n). */

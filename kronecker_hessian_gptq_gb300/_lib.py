@@ -23,6 +23,7 @@ STATUS_NAMES = {
 DEV_NONFINITE_W = 1
 DEV_BAD_SCALE = 2
 DEV_TIMEOUT = 4
+KERNEL_CLASSES = ("setup", "tile_solve", "propagate")
 
 _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
@@ -39,6 +40,8 @@ SIGNATURES = {
     "bakron_prepare": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_workspace_size": (_sz, [_i64, _i64]),
     "bakron_quantize": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "bakron_quantize_profile": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp,
+                                        _vp, _vp, _vp]),
     "bakron_quantize_host_workspace_size": (_sz, [_i64, _i64]),
     "bakron_quantize_host": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
 }

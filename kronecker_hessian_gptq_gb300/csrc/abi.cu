@@ -87,6 +87,30 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
                                            (cudaStream_t)stream));
 }
 
+int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                            int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                            int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,
+                            double* kernel_flops) {
+  if (!kernel_ms || !kernel_launches || !kernel_flops) return BAKRON_ERR_INVALID_ARG;
+  if (!W || !LA || !LB || !V || !Wq || !status_dev) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if (!(bits == 0 || (bits >= 2 && bits <= 8))) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)Wq == (const void*)W || (const void*)V == (const void*)W || (void*)V == (void*)Wq)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  bakron::KernelTimer t;
+  cudaError_t e = bakron::quantize_launch(W, LA, LB, scales, bits, (int)m, (int)n, V, Wq, ws, status_dev,
+                                          (cudaStream_t)stream, &t);
+  if (e != cudaSuccess) return BAKRON_ERR_CUDA;
+  for (int c = 0; c < bakron::kKernelClasses; ++c) {
+    kernel_ms[c] = t.ms[c];
+    kernel_launches[c] = t.launches[c];
+    kernel_flops[c] = t.flops[c];
+  }
+  return BAKRON_OK;
+}
+
 size_t bakron_quantize_host_workspace_size(int64_t m, int64_t n) {
   if (m < 1 || n < 1 || m * n >= kMaxElems) return 0;
   using bakron::align_up;

@@ -11,11 +11,20 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Per-kernel-class timing of one solve (diagnostics): CUDA events around
+// every launch, read back after the stream is synchronized.
+constexpr int kKernelClasses = 3;  // 0: prepass + offset, 1: tile solve, 2: propagate
+struct KernelTimer {
+  double ms[kKernelClasses];
+  int64_t launches[kKernelClasses];
+  double flops[kKernelClasses];  // algorithmic flops (2 per multiply-add) of the class
+};
+
 // quantize.cu
 size_t quantize_workspace_bytes(int64_t m, int64_t n);
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
                             int bits, int m, int n, int32_t* V, float* Wq, void* ws,
-                            int32_t* status_dev, cudaStream_t stream);
+                            int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
 
 // prep.cu
 size_t factor_workspace_bytes(int64_t d);

@@ -37,6 +37,7 @@
 // (df.cuh); the rounding decision itself is the fp32 division
 // fp32(W~) / s_i rounded half to even, and E = s_i v - W~ is formed exactly.
 #include <algorithm>
+#include <vector>
 
 #include "bakron.h"
 #include "df.cuh"
@@ -270,9 +271,66 @@ size_t quantize_workspace_bytes(int64_t m, int64_t n) {
   return sizeof(Header) + 3 * plane;
 }
 
+// Event pairs around launches when a KernelTimer is given.
+class LaunchClock {
+ public:
+  LaunchClock(KernelTimer* t, cudaStream_t s) : t_(t), s_(s) {
+    if (t_) {
+      for (int c = 0; c < kKernelClasses; ++c) {
+        t_->ms[c] = 0.0;
+        t_->launches[c] = 0;
+        t_->flops[c] = 0.0;
+      }
+    }
+  }
+  ~LaunchClock() {
+    for (auto& r : recs_) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+  }
+  void begin(int cls) {
+    if (!t_) return;
+    Rec r;
+    r.cls = cls;
+    cudaEventCreate(&r.a);
+    cudaEventCreate(&r.b);
+    cudaEventRecord(r.a, s_);
+    recs_.push_back(r);
+  }
+  void end(double flops) {
+    if (!t_) return;
+    Rec& r = recs_.back();
+    cudaEventRecord(r.b, s_);
+    t_->launches[r.cls] += 1;
+    t_->flops[r.cls] += flops;
+  }
+  cudaError_t finish() {
+    if (!t_) return cudaSuccess;
+    cudaError_t e = cudaStreamSynchronize(s_);
+    if (e != cudaSuccess) return e;
+    for (auto& r : recs_) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, r.a, r.b);
+      if (e != cudaSuccess) return e;
+      t_->ms[r.cls] += ms;
+    }
+    return cudaSuccess;
+  }
+
+ private:
+  struct Rec {
+    int cls;
+    cudaEvent_t a, b;
+  };
+  KernelTimer* t_;
+  cudaStream_t s_;
+  std::vector<Rec> recs_;
+};
+
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
                             int bits, int m, int n, int32_t* V, float* Wq, void* ws,
-                            int32_t* status_dev, cudaStream_t stream) {
+                            int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
   const size_t plane = align_up((size_t)m * (size_t)n * sizeof(float2));
   char* base = static_cast<char*>(ws);
   QParams P;
@@ -295,23 +353,35 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.lo = bits ? -(1 << (bits - 1)) : 0;
   P.hi = bits ? (1 << (bits - 1)) - 1 : 0;
 
+  LaunchClock clock(timer, stream);
   cudaError_t err = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
   if (err != cudaSuccess) return err;
   err = cudaMemsetAsync(P.hdr, 0, sizeof(Header), stream);
   if (err != cudaSuccess) return err;
   const size_t total = (size_t)m * n;
   const int pre_blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
+  clock.begin(0);
   prepass_kernel<<<pre_blocks, 256, 0, stream>>>(P);
   sigma_kernel<<<1, 1, 0, stream>>>(P);
+  clock.end(0.0);
+  const double t3 = (double)T * T * T;
   for (int K = 0; K <= P.Mt + P.Nt - 2; ++K) {
     const int I0 = K - (P.Nt - 1) > 0 ? K - (P.Nt - 1) : 0;
     const int I1 = K < P.Mt - 1 ? K : P.Mt - 1;
     const int nsrc = I1 - I0 + 1;
+    clock.begin(1);
     tile_solve_kernel<<<nsrc, dim3(T, T), 0, stream>>>(P, K, I0);
+    clock.end(2.0 * 1.5 * t3 * nsrc);  // in-tile row and column sums + L_B[I,I] Gx
     const int ntgt = P.Mt + P.Nt - 2 - K;
-    if (ntgt > 0) propagate_kernel<<<dim3(nsrc, ntgt), 256, 0, stream>>>(P, K, I0);
+    if (ntgt > 0) {
+      clock.begin(2);
+      propagate_kernel<<<dim3(nsrc, ntgt), 256, 0, stream>>>(P, K, I0);
+      clock.end(2.0 * t3 * (double)nsrc * ntgt);
+    }
   }
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  return clock.finish();
 }
 
 }  // namespace bakron

