@@ -163,6 +163,33 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
                          int bits, int64_t m, int64_t n, int32_t* V, float* Wq, void* dev_ws,
                          size_t dev_ws_bytes, int32_t* status_host, void* stream);
 
+/* ------------------------------------------------------- no-allocation solve
+ * For callers that cannot allocate device memory at all: a plugin inside a
+ * host application whose device memory is entirely owned by another
+ * allocator, or a latency-critical path that must not call cudaMalloc
+ * (which can synchronize the whole device).  The paper has no counterpart;
+ * this is an interface convenience.
+ *
+ * Same computation and arguments as bakron_quantize, without `ws`: the
+ * scratch space comes from a fixed array inside the library, of
+ * BAKRON_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
+ * until the process exits.  The caller still passes (and owns) W, LA, LB,
+ * scales, V, Wq and status_dev.  Sizes with
+ * bakron_quantize_workspace_size(m, n) > BAKRON_NOALLOC_SCRATCH_BYTES
+ * (about 2.79 million weights, e.g. 1024 x 2048) are rejected with
+ * BAKRON_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  The call allocates nothing.
+ * Every call on a device shares the one array and leaves its contents
+ * behind; each call re-initializes what it reads, but calls that overlap on
+ * the GPU (other streams, other host threads) race on it: serialize them.
+ */
+#define BAKRON_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int bakron_quantize_noalloc(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                            int64_t m, int64_t n, int32_t* V, float* Wq, int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

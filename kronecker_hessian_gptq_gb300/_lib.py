@@ -44,6 +44,7 @@ SIGNATURES = {
                                         _vp, _vp, _vp]),
     "bakron_quantize_host_workspace_size": (_sz, [_i64, _i64]),
     "bakron_quantize_host": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "bakron_quantize_noalloc": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
