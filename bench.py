@@ -238,9 +238,10 @@ def run_ours(args, rank, local_rank, world):
     total_ms = aggregate_max(sum(step_ms), world, dev)
 
     # Per-kernel timing pass (events around every launch), after the timed region.
-    kms = (ctypes.c_double * 3)()
-    kl = (ctypes.c_int64 * 3)()
-    kf = (ctypes.c_double * 3)()
+    ncls = len(_lib.KERNEL_CLASSES)
+    kms = (ctypes.c_double * ncls)()
+    kl = (ctypes.c_int64 * ncls)()
+    kf = (ctypes.c_double * ncls)()
     for _ in range(2):
         flush.zero_()
         st = lib.bakron_quantize_profile(W.data_ptr(), LA.data_ptr(), LB.data_ptr(), None if s is None else s.data_ptr(),
@@ -249,8 +250,8 @@ def run_ours(args, rank, local_rank, world):
         _lib.check(st, "bakron_quantize_profile")
     kernels = {name: {"ms": kms[c], "launches": kl[c], "alg_tflops": (kf[c] / (kms[c] * 1e-3) / 1e12) if kms[c] else 0}
                for c, name in enumerate(_lib.KERNEL_CLASSES)}
-    dom = max(range(3), key=lambda c: kms[c])
-    launches_per_step = 2 * kl[0] + kl[1] + kl[2]
+    dom = max(range(ncls), key=lambda c: kms[c])
+    launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
 
     # End to end through the host entry point: pinned host inputs in, codes out.
     Wh = torch.from_numpy(p.W).pin_memory()

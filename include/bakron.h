@@ -138,11 +138,12 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
  * (host memory) receiving, per kernel class, the summed event time in ms,
  * the number of launches and the algorithmic flops (2 per multiply-add of
  * the products L_B E L_A^T the class computes).  Classes: 0 = input
- * check and state set-up, 1 = tile solve (diagonal blocks), 2 = forward
- * propagation (off-diagonal blocks).  Synchronizes `stream` before it
- * returns; the events add a little time to every launch.
+ * check and set-up, 1 = tile solve (diagonal blocks and the distance-1
+ * neighbours), 2 = mid pushes (single source tiles), 3 = chunk pushes
+ * (batched source tiles).  Synchronizes `stream` before it returns; the
+ * events add a little time to every launch.
  */
-#define BAKRON_KERNEL_CLASSES 3
+#define BAKRON_KERNEL_CLASSES 4
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,
@@ -176,7 +177,7 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
  * until the process exits.  The caller still passes (and owns) W, LA, LB,
  * scales, V, Wq and status_dev.  Sizes with
  * bakron_quantize_workspace_size(m, n) > BAKRON_NOALLOC_SCRATCH_BYTES
- * (about 2.79 million weights, e.g. 1024 x 2048) are rejected with
+ * (about 1.39 million weights, e.g. 1024 x 1024) are rejected with
  * BAKRON_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on a device looks up the array's device address for that

@@ -23,7 +23,7 @@ STATUS_NAMES = {
 DEV_NONFINITE_W = 1
 DEV_BAD_SCALE = 2
 DEV_TIMEOUT = 4
-KERNEL_CLASSES = ("setup", "tile_solve", "propagate")
+KERNEL_CLASSES = ("setup", "tile_solve", "mid_push", "chunk_push")
 
 _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t

@@ -13,7 +13,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Per-kernel-class timing of one solve (diagnostics): CUDA events around
 // every launch, read back after the stream is synchronized.
-constexpr int kKernelClasses = 3;  // 0: prepass + offset, 1: tile solve, 2: propagate
+constexpr int kKernelClasses = 4;  // 0: input check + offset, 1: tile solve, 2: mid push, 3: chunk push
 struct KernelTimer {
   double ms[kKernelClasses];
   int64_t launches[kKernelClasses];
