@@ -319,56 +319,111 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   }
 }
 
-// Shared memory of one push CTA: the factor block of up to U*T target rows
-// by T source columns, in its natural [row][k] layout (float4 reads along k,
-// all lanes of a warp reading the same rows, or rows 36 floats apart), and
-// one source tile.
+// ---- asynchronous global -> shared copies (cp.async, zero-filled past the end)
+__device__ __forceinline__ void cp_async(void* smem, const void* gmem, int src_bytes, int cp_bytes) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  if (cp_bytes == 16) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+  } else if (cp_bytes == 8) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+  } else {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+  }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+
+// Shared memory of one push CTA (dynamic): NS stages of the factor block of
+// up to U*T target rows by T source columns in its natural [row][k] layout
+// (float4 reads along k) and of one source tile.  Mid pushes use one stage
+// (a small footprint that fits beside the other kernels), chunk products two
+// (the next source tile is copied in while the current one is used).
+template <int NS>
 struct PushSmem {
-  float L[U * T][T + 4];
-  float2 S[T][T + 2];
+  float L[NS][U * T][T + 4];
+  float2 S[NS][T][T + 2];
 };
+
+// Stages factor block rows [r0, r0 + U*T) x columns [k0, k0 + T) of the
+// row-major d x d factor F (rows >= rows_valid or >= d, columns >= d: zero).
+__device__ __forceinline__ void stage_factor(float (*dst)[T + 4], const float* F, int d, int r0, int rows_valid,
+                                             int k0) {
+  if ((d % 4) == 0) {  // 16-byte aligned rows
+    for (int e = threadIdx.x; e < U * T * (T / 4); e += blockDim.x) {
+      const int rr = e / (T / 4), k = 4 * (e % (T / 4));
+      const int gr = r0 + rr, gk = k0 + k;
+      const bool ok = rr < rows_valid && gr < d && gk < d;
+      cp_async(&dst[rr][k], ok ? (const void*)(F + (size_t)gr * d + gk) : (const void*)F,
+               ok ? 4 * min(4, d - gk) : 0, 16);
+    }
+  } else {
+    for (int e = threadIdx.x; e < U * T * T; e += blockDim.x) {
+      const int rr = e / T, k = e % T;
+      const int gr = r0 + rr, gk = k0 + k;
+      const bool ok = rr < rows_valid && gr < d && gk < d;
+      cp_async(&dst[rr][k], ok ? (const void*)(F + (size_t)gr * d + gk) : (const void*)F, ok ? 4 : 0, 4);
+    }
+  }
+}
+
+// Stages the T x T double-float tile rows [r0, r0+T) x columns [c0, c0+T) of
+// the m x n plane M (outside the matrix: zero).
+__device__ __forceinline__ void stage_tile(float2 (*dst)[T + 2], const float2* M, int m, int n, int r0, int c0) {
+  for (int e = threadIdx.x; e < T * T; e += blockDim.x) {
+    const int rr = e / T, cc = e % T;
+    const int gr = r0 + rr, gc = c0 + cc;
+    const bool ok = gr < m && gc < n;
+    cp_async(&dst[rr][cc], ok ? (const void*)(M + (size_t)gr * n + gc) : (const void*)M, ok ? 8 : 0, 8);
+  }
+}
 
 // Column push: X[tiles tr0 .. tr0+ntr-1, column tile J] +=
 //   L_B[those rows, source tile rows sr0 .. sr0+nsr-1] * G[source rows, column tile J].
 // Lane l owns column l; warp w owns the 16 rows 16w .. 16w+15 (coalesced
 // read-modify-write of 32 consecutive double-floats per row).
-__device__ void column_push(const QParams& P, PushSmem& sm, float2* X, int J, int tr0, int ntr, int sr0, int nsr,
-                            float sigma) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <int NS>
+__device__ void column_push(const QParams& P, PushSmem<NS>& sm, float2* X, int J, int tr0, int ntr, int sr0,
+                            int nsr, float sigma) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int R = U * T / 8;  // rows per warp (16)
   const int rbase = R * warp;
   OffsetAcc acc[R];
 #pragma unroll
   for (int u = 0; u < R; ++u) acc[u].init(sigma);
   const int rows = ntr * T;
-  const int gc = J * T + lane;
   for (int st = 0; st < nsr; ++st) {
-    const int sbase = (sr0 + st) * T;  // first source row
-    __syncthreads();
-    for (int e = tid; e < U * T * T; e += blockDim.x) {
-      const int rr = e / T, k = e % T;
-      const int gr = tr0 * T + rr, gk = sbase + k;
-      sm.L[rr][k] = (rr < rows && gr < P.m && gk < P.m) ? P.LB[(size_t)gr * P.m + gk] : 0.f;
+    const int buf = NS == 1 ? 0 : (st & 1);
+    if (NS == 1 || st == 0) {
+      stage_factor(sm.L[buf], P.LB, P.m, tr0 * T, rows, (sr0 + st) * T);
+      stage_tile(sm.S[buf], P.G, P.m, P.n, (sr0 + st) * T, J * T);
+      cp_async_commit();
     }
-    for (int e = tid; e < T * T; e += blockDim.x) {
-      const int k = e / T, qq = e % T;
-      const int gk = sbase + k, gcc = J * T + qq;
-      sm.S[k][qq] = (gk < P.m && gcc < P.n) ? P.G[(size_t)gk * P.n + gcc] : make_float2(0.f, 0.f);
+    if (NS == 2 && st + 1 < nsr) {
+      stage_factor(sm.L[buf ^ 1], P.LB, P.m, tr0 * T, rows, (sr0 + st + 1) * T);
+      stage_tile(sm.S[buf ^ 1], P.G, P.m, P.n, (sr0 + st + 1) * T, J * T);
+      cp_async_commit();
+      cp_async_wait_all_but_one();
+    } else {
+      cp_async_wait_all();
     }
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < T; k += 4) {
-      const float2 g0 = sm.S[k][lane], g1 = sm.S[k + 1][lane], g2 = sm.S[k + 2][lane], g3 = sm.S[k + 3][lane];
+      const float2 g0 = sm.S[buf][k][lane], g1 = sm.S[buf][k + 1][lane];
+      const float2 g2 = sm.S[buf][k + 2][lane], g3 = sm.S[buf][k + 3][lane];
 #pragma unroll
       for (int u = 0; u < R; ++u) {
-        const float4 a = *reinterpret_cast<const float4*>(&sm.L[rbase + u][k]);
+        const float4 a = *reinterpret_cast<const float4*>(&sm.L[buf][rbase + u][k]);
         acc[u].mac(a.x, g0);
         acc[u].mac(a.y, g1);
         acc[u].mac(a.z, g2);
         acc[u].mac(a.w, g3);
       }
     }
+    __syncthreads();
   }
+  const int gc = J * T + lane;
   if (gc >= P.n) return;
 #pragma unroll
   for (int u = 0; u < R; ++u) {
@@ -383,9 +438,10 @@ __device__ void column_push(const QParams& P, PushSmem& sm, float2* X, int J, in
 // Row push: Gp[row tile I, tiles tc0 .. tc0+ntc-1] +=
 //   E[row tile I, source tile columns sc0 .. sc0+nsc-1] * L_A[target rows, source columns]^T.
 // Lane l owns the columns l, l+32, l+64, l+96; warp w owns rows 4w .. 4w+3.
-__device__ void row_push(const QParams& P, PushSmem& sm, float2* Gp, int I, int tc0, int ntc, int sc0, int nsc,
-                         float sigma) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <int NS>
+__device__ void row_push(const QParams& P, PushSmem<NS>& sm, float2* Gp, int I, int tc0, int ntc, int sc0,
+                         int nsc, float sigma) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int p0 = 4 * warp;
   OffsetAcc acc[4][U];
 #pragma unroll
@@ -394,28 +450,30 @@ __device__ void row_push(const QParams& P, PushSmem& sm, float2* Gp, int I, int 
     for (int v = 0; v < U; ++v) acc[u][v].init(sigma);
   const int cols = ntc * T;
   for (int st = 0; st < nsc; ++st) {
-    const int sbase = (sc0 + st) * T;  // first source column
-    __syncthreads();
-    for (int e = tid; e < U * T * T; e += blockDim.x) {
-      const int cc = e / T, k = e % T;  // target column (row of L_A), source column
-      const int gr = tc0 * T + cc, gk = sbase + k;
-      sm.L[cc][k] = (cc < cols && gr < P.n && gk < P.n) ? P.LA[(size_t)gr * P.n + gk] : 0.f;
+    const int buf = NS == 1 ? 0 : (st & 1);
+    if (NS == 1 || st == 0) {
+      stage_factor(sm.L[buf], P.LA, P.n, tc0 * T, cols, (sc0 + st) * T);
+      stage_tile(sm.S[buf], P.E, P.m, P.n, I * T, (sc0 + st) * T);
+      cp_async_commit();
     }
-    for (int e = tid; e < T * T; e += blockDim.x) {
-      const int pp = e / T, k = e % T;
-      const int gr = I * T + pp, gk = sbase + k;
-      sm.S[pp][k] = (gr < P.m && gk < P.n) ? P.E[(size_t)gr * P.n + gk] : make_float2(0.f, 0.f);
+    if (NS == 2 && st + 1 < nsc) {
+      stage_factor(sm.L[buf ^ 1], P.LA, P.n, tc0 * T, cols, (sc0 + st + 1) * T);
+      stage_tile(sm.S[buf ^ 1], P.E, P.m, P.n, I * T, (sc0 + st + 1) * T);
+      cp_async_commit();
+      cp_async_wait_all_but_one();
+    } else {
+      cp_async_wait_all();
     }
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < T; k += 4) {
       float4 lv[U];
 #pragma unroll
-      for (int v = 0; v < U; ++v) lv[v] = *reinterpret_cast<const float4*>(&sm.L[lane + T * v][k]);
+      for (int v = 0; v < U; ++v) lv[v] = *reinterpret_cast<const float4*>(&sm.L[buf][lane + T * v][k]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float4 e01 = *reinterpret_cast<const float4*>(&sm.S[p0 + u][k]);
-        const float4 e23 = *reinterpret_cast<const float4*>(&sm.S[p0 + u][k + 2]);
+        const float4 e01 = *reinterpret_cast<const float4*>(&sm.S[buf][p0 + u][k]);
+        const float4 e23 = *reinterpret_cast<const float4*>(&sm.S[buf][p0 + u][k + 2]);
         const float2 e0 = make_float2(e01.x, e01.y), e1 = make_float2(e01.z, e01.w);
         const float2 e2 = make_float2(e23.x, e23.y), e3 = make_float2(e23.z, e23.w);
 #pragma unroll
@@ -427,6 +485,7 @@ __device__ void row_push(const QParams& P, PushSmem& sm, float2* Gp, int I, int 
         }
       }
     }
+    __syncthreads();
   }
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -447,7 +506,8 @@ __device__ void row_push(const QParams& P, PushSmem& sm, float2* Gp, int I, int 
 // Mid pushes of the sources of tile anti-diagonal K (blockIdx.x: source
 // I = I0 + blockIdx.x; blockIdx.y: group of U targets, column targets first).
 __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0) {
-  __shared__ __align__(16) PushSmem sm;
+  extern __shared__ __align__(16) unsigned char push_smem[];
+  PushSmem<1>& sm = *reinterpret_cast<PushSmem<1>*>(push_smem);
   const int I = I0 + blockIdx.x, J = K - I;
   const int c_first = I + 2, c_end = min(P.Mt, mid_end(I));
   const int r_first = J + 2, r_end = min(P.Nt, mid_end(J));
@@ -464,13 +524,16 @@ __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0)
   }
 }
 
+// (At most 85 registers per thread: three chunk CTAs fit in the register
+// file, so a tile solve finds room beside two.)
 // Chunk products launched once tile anti-diagonal K is solved: for every
 // column J whose tile (K - J, J) closes a chunk of B tile rows, and every row
 // I whose tile (I, K - I) closes a chunk of B tile columns.  blockIdx.x:
 // candidate (columns first, J = K - (B-1) - B*t, then rows likewise);
 // blockIdx.y: group of U targets.
-__global__ void __launch_bounds__(256) chunk_push_kernel(QParams P, int K, int ncand_col) {
-  __shared__ __align__(16) PushSmem sm;
+__global__ void __launch_bounds__(256, 3) chunk_push_kernel(QParams P, int K, int ncand_col) {
+  extern __shared__ __align__(16) unsigned char push_smem[];
+  PushSmem<2>& sm = *reinterpret_cast<PushSmem<2>*>(push_smem);
   const float sigma = P.hdr->sigma;
   const int t = blockIdx.x, u = blockIdx.y;
   if (t < ncand_col) {
@@ -556,9 +619,12 @@ class LaunchClock {
 // every call.  Streams and events are driver objects, not device memory.
 // Calls that share a set serialize their side work on its streams, which
 // is correct: each call's main stream waits only on its own events' records.
-// Unused dynamic shared memory that caps chunk CTAs at two per SM, so that
-// every SM keeps room for a tile solve and a mid push beside them.
-constexpr int kChunkPadSmem = 50 * 1024;
+// Dynamic shared memory: a mid push CTA holds one stage; a chunk CTA holds
+// two stages and asks for unused extra space that caps chunk CTAs at two
+// per SM, so that every SM keeps room for a tile solve and a mid push.
+constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
+constexpr int kChunkSmem = 76 * 1024;
+static_assert(kChunkSmem >= (int)sizeof(PushSmem<2>), "two push stages fit");
 
 struct StreamSet {
   bool ready = false;
@@ -579,7 +645,7 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     if (e != cudaSuccess) return e;
     e = cudaStreamCreateWithPriority(&S.chunk, cudaStreamNonBlocking, lo);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_push_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkPadSmem);
+    e = cudaFuncSetAttribute(chunk_push_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
     if (e != cudaSuccess) return e;
     S.ready = true;
   }
@@ -691,7 +757,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
       cudaStreamWaitEvent(s_mid, ev_solve[K], 0);
       const int units = 2 * ((2 * B - 2 + U - 1) / U);
       clock.begin(2, s_mid);
-      mid_push_kernel<<<dim3(nsrc, units), 256, 0, s_mid>>>(P, K, I0);
+      mid_push_kernel<<<dim3(nsrc, units), 256, kMidSmem, s_mid>>>(P, K, I0);
       clock.end(2.0 * t3 * mid_tiles);
       cudaEventRecord(ev_mid[K], s_mid);
       mid_on[K] = 1;
@@ -714,7 +780,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
       cudaStreamWaitEvent(s_chunk, ev_solve[K], 0);
       const int units = (std::max(P.Mt, P.Nt) + U - 1) / U;
       clock.begin(3, s_chunk);
-      chunk_push_kernel<<<dim3(ncc + ncr, units), 256, kChunkPadSmem, s_chunk>>>(P, K, ncc);
+      chunk_push_kernel<<<dim3(ncc + ncr, units), 256, kChunkSmem, s_chunk>>>(P, K, ncc);
       clock.end(2.0 * B * t3 * chunk_tiles);
       cudaEventRecord(ev_chunk[K], s_chunk);
       chunk_on[K] = 1;
