@@ -177,8 +177,8 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
  * until the process exits.  The caller still passes (and owns) W, LA, LB,
  * scales, V, Wq and status_dev.  Sizes with
  * bakron_quantize_workspace_size(m, n) > BAKRON_NOALLOC_SCRATCH_BYTES
- * (about 72 bytes per weight for square layers: up to about 950 x 950)
- * are rejected with
+ * (48 bytes of solver state per weight: up to about 1.39 million weights,
+ * e.g. 1024 x 1024) are rejected with
  * BAKRON_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on a device looks up the array's device address for that

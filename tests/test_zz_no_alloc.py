@@ -75,10 +75,10 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(env):
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(env):
     bk, lib, torch = env
-    m, n = 1024, 1024  # about 72 MiB of solver state
+    m, n = 2048, 2048  # 192 MiB of solver state
     assert bk.quantize_workspace_size(m, n) > SCRATCH_BYTES
     fake = ctypes.c_void_p(0x1000)
     rc = lib.bakron_quantize_noalloc(fake, fake, fake, None, 4, m, n, ctypes.c_void_p(0x2000),
                                      ctypes.c_void_p(0x3000), fake, None)
     assert rc == 4  # BAKRON_ERR_WORKSPACE, returned before anything is enqueued
-    assert bk.quantize_workspace_size(900, 900) <= SCRATCH_BYTES
+    assert bk.quantize_workspace_size(1024, 1024) <= SCRATCH_BYTES
