@@ -641,9 +641,13 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     int lo = 0, hi = 0;
     e = cudaDeviceGetStreamPriorityRange(&lo, &hi);  // hi is the most urgent (numerically lowest)
     if (e != cudaSuccess) return e;
+    // Both side streams get the highest priority: the chunk products are
+    // the largest block of work and their stream sets the pace (measured on
+    // c3: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms here).
+    (void)lo;
     e = cudaStreamCreateWithPriority(&S.mid, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
-    e = cudaStreamCreateWithPriority(&S.chunk, cudaStreamNonBlocking, lo);
+    e = cudaStreamCreateWithPriority(&S.chunk, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chunk_push_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
     if (e != cudaSuccess) return e;
