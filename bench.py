@@ -183,6 +183,39 @@ def measured_peaks() -> dict:
         return {}
 
 
+KERNEL_SOURCES = ("kronecker_hessian_gptq_gb300/csrc/quantize.cu", "kronecker_hessian_gptq_gb300/csrc/df.cuh")
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the sources the solve kernels are compiled from."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` (dram__bytes_read.sum +
+    dram__bytes_write.sum, averaged over the captured launches), as recorded in
+    the ncu summary profiles/<kernel>_<workload>_dram.md.  None when there is no
+    such summary or the kernel sources changed since it was captured."""
+    import re
+
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_dram.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    b = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
+    d = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    if not b or not d or d.group(1) != kernel_source_digest():
+        return None
+    return int(b.group(1))
+
+
 def run_ours(args, rank, local_rank, world):
     import ctypes
 
@@ -284,7 +317,8 @@ def run_ours(args, rank, local_rank, world):
         "solve_alg_tflops": f_alg / (total_ms / args.steps * 1e-3) / 1e12,
         "prep_ms": prep_ms,
         "roofline": {"bound": "alu", "kernel": _lib.KERNEL_CLASSES[dom], "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic(_lib.KERNEL_CLASSES[dom], p.name.split("_")[0]),
                      "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_max:.0f} MHz / "
                                    f"{DF_INSTR_PER_MAC} instr per double-float MAC x 2 flops"},
         "kernels": kernels,

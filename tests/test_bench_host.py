@@ -82,3 +82,23 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch):
     c = bench.ClockSampler(0)
     c.start()
     assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    import shutil
+
+    import bench
+
+    for rel in bench.KERNEL_SOURCES:
+        os.makedirs(tmp_path / os.path.dirname(rel), exist_ok=True)
+        shutil.copy(os.path.join(ROOT, rel), tmp_path / rel)
+    os.makedirs(tmp_path / "profiles")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("chunk_push", "c3") is None  # no summary
+    digest = bench.kernel_source_digest()
+    (tmp_path / "profiles" / "chunk_push_c3_dram.md").write_text(
+        f"# summary\ntraffic_bytes_per_launch: 123456\nsource_sha256: {digest}\n")
+    assert bench.profiled_traffic("chunk_push", "c3") == 123456
+    with open(tmp_path / bench.KERNEL_SOURCES[0], "a") as f:
+        f.write("\n// edited\n")
+    assert bench.profiled_traffic("chunk_push", "c3") is None  # stale once the kernel changes
