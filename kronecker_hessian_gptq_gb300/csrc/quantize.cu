@@ -42,6 +42,8 @@
 // Precision: every accumulation is double-float (df.cuh); the rounding
 // decision is the fp32 quotient fp32(W~) / s_i rounded half to even, with the
 // correctly rounded division used whenever the quotient is near a tie.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -82,7 +84,15 @@ struct QParams {
   float2* E;   // errors at rounding time
   Header* hdr;
   int32_t* status;
-  int m, n, Mt, Nt, bits, lo, hi;
+  const __nv_bfloat16* digA;  // digits of L_A and L_B (chunk products)
+  const __nv_bfloat16* digB;
+  const signed char* expA;    // their (row, chunk) exponents
+  const signed char* expB;
+  __nv_bfloat16* DE;          // digits of E, [digit][row][ldE], ldE = n rounded up to 8
+  __nv_bfloat16* DGt;         // digits of G transposed, [digit][col][ldG], ldG = m rounded up to 8
+  size_t dstrideE, dstrideG;  // elements per digit plane
+  int ldE, ldG;
+  int m, n, Mt, Nt, bits, lo, hi, nchA, nchB;
 };
 
 __device__ __forceinline__ unsigned warp_max(unsigned v) {
@@ -130,6 +140,37 @@ __global__ void sigma_kernel(QParams P) {
   // Every value rounded or accumulated stays within a few alphabet steps of
   // the weights; the offset leaves a wide margin above that.
   P.hdr->sigma = offset_for_bound(16.f * (maxw + maxs * (levels + 2.f)));
+}
+
+// Exponent e with |x| < 2^e for every |x| <= mx, kept >= -100 so that every
+// scale 2^(7 - e) below is a normal float (smaller values are negligible
+// against the offset of the accumulators).
+__device__ __forceinline__ int bound_exp(float mx) {
+  if (!(mx > 0.f)) return -100;
+  int e;
+  frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1)
+  return max(e, -100);
+}
+
+// 2^k as a float, -126 <= k <= 127.
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((k + 127) << 23); }
+
+
+// Source digits (the B operand of the chunk products, see the tensor-core
+// section below): six bf16 integer digits of a double-float value x on the
+// global exponent eD of the solve (2^eD = 2 sigma exceeds every value the
+// solve holds, since the offset accumulators rely on that bound):
+//   x ~ 2^(eD-7) sum_{b<6} d_b 256^-b,  |d_b| <= 128, error <= 2^(eD-48).
+constexpr int kDigD = 6;
+__device__ __forceinline__ void put_digits(__nv_bfloat16* planes, size_t pstride, size_t o, float2 x, float sc) {
+  float2 u = make_float2(x.x * sc, x.y * sc);
+#pragma unroll
+  for (int b = 0; b < kDigD; ++b) {
+    const float dg = rintf(u.x);
+    planes[b * pstride + o] = __float2bfloat16_rn(dg);
+    const float2 rem = two_sum(u.x - dg, u.y);
+    u = make_float2(rem.x * 256.f, rem.y * 256.f);
+  }
 }
 
 // Source tile index s lies in chunk s / B; it pushes itself to the targets
@@ -306,16 +347,30 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     }
   }
   __syncthreads();
+  const float dsc = pow2f(7 - bound_exp(sigma));
+  float2 gv[kPer];
 #pragma unroll
   for (int t = 0; t < kPer; ++t) {  // natural mapping again: coalesced stores of E and G
     const int a = warp + kRows * t;
     const int ra = I * T + a;
+    const float2 e = sB[a][b];
+    gv[t] = df_add(sGx[a][b], df_add(sA[a][b], e));
     if (ra < P.m && vb) {
       const size_t o = (size_t)ra * P.n + cb;
-      const float2 e = sB[a][b];
       P.E[o] = e;
-      P.G[o] = df_add(sGx[a][b], df_add(sA[a][b], e));
+      P.G[o] = gv[t];
+      put_digits(P.DE, P.dstrideE, (size_t)ra * P.ldE + cb, e, dsc);
     }
+  }
+  __syncthreads();  // every read of sGx above is done
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) sGx[warp + kRows * t][b] = gv[t];
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {  // G digits transposed: lane = row, coalesced along the row
+    const int col = warp + kRows * t, row = lane;
+    const int gr = I * T + row, gc = J * T + col;
+    if (gr < P.m && gc < P.n) put_digits(P.DGt, P.dstrideG, (size_t)gc * P.ldG + gr, sGx[row][col], dsc);
   }
 }
 
@@ -524,36 +579,282 @@ __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0)
   }
 }
 
-// (At most 85 registers per thread: three chunk CTAs fit in the register
-// file.)
-// Chunk products launched once tile anti-diagonal K is solved: for every
-// column J whose tile (K - J, J) closes a chunk of B tile rows, and every row
-// I whose tile (I, K - I) closes a chunk of B tile columns.  blockIdx.x:
-// candidate (columns first, J = K - (B-1) - B*t, then rows likewise);
-// blockIdx.y: group of U targets.
-__global__ void __launch_bounds__(256, 3) chunk_push_kernel(QParams P, int K, int ncand_col) {
-  extern __shared__ __align__(16) unsigned char push_smem[];
-  PushSmem<2>& sm = *reinterpret_cast<PushSmem<2>*>(push_smem);
-  const float sigma = P.hdr->sigma;
-  const int t = blockIdx.x, u = blockIdx.y;
-  if (t < ncand_col) {
-    const int J = K - (B - 1) - B * t;      // the chunk's last tile row is K - J = B - 1 + B t
-    const int last = K - J;
-    if (J < 0 || J >= P.Nt || last >= P.Mt) return;
-    const int c = last / B;
-    const int first = (c + 2) * B;
-    const int ntiles = P.Mt - first;
-    if (ntiles <= 0 || u * U >= ntiles) return;
-    column_push(P, sm, P.Xc, J, first + u * U, min(U, ntiles - u * U), c * B, B, sigma);
+// ---- Chunk products on the tensor cores, by an exact digit split (after
+// Ozaki, Ogita, Oishi and Rump, "Error-free transformations of matrix
+// multiplication by using fast routines of matrix multiplication and its
+// applications", Numer. Algorithms 2012).
+//
+// A chunk product is Y (UC*T x T) = F (UC*T x CK) * D (CK x T): F a block of a
+// factor (fp32), D a source block of G or E^T (double-float), CK = B*T.
+// With e_r bounding row r of F over the chunk (|F[r][k]| < 2^e_r) and e_q
+// bounding column q of D,
+//   F[r][k] ~ 2^(e_r-7) sum_{a<5} f_a[r][k] 256^-a,
+//   D[k][q] ~ 2^(e_q-7) sum_{b<6} d_b[k][q] 256^-b,
+// with integer digits |f_a|, |d_b| <= 128, exact in bf16.  Five digits hold
+// every factor element whose magnitude is at least 2^-16 of its row's bound
+// exactly (an fp32 significand has 24 bits) and the others to 2^-40 of the
+// bound; six digits hold a double-float to 48 bits.  (Four factor digits
+// leave an error near 1e-9 of sum |F||D| on factor rows whose entries span
+// a few binades; five leave 6e-13.)  Every digit product is exact, and per
+// level l = a + b the sum over k and over the <= 5 pairs of the level stays
+// below 5 * 128 * 128^2 < 2^24, so fp32 tensor-core accumulation of each
+// level is exact.  The 20 pairs of levels 0..5 are kept (the dropped ones
+// are below 2^-48 of row bound times column bound); the levels are summed
+// in double-float and scaled by 2^(e_r + e_q - 14).
+constexpr int CK = B * T;     // chunk depth (128)
+constexpr int kDigF = 5;      // digits of a factor element
+constexpr int kLevels = 6;    // levels 0 .. kDigD - 1
+constexpr int kSlab = 32;     // k-slab of factor digits staged at once
+constexpr int UC = 2;         // target tiles per chunk product CTA
+constexpr int kTcRowWarps = UC * T / 16;
+constexpr int kTcThreads = 2 * kTcRowWarps * 32;  // warps of 16 x 16 outputs
+
+// Exponent of every (row, chunk) block of a d x d factor: out[r * nch + c]
+// bounds row r over columns [c*CK, (c+1)*CK).  One warp per block.
+__global__ void __launch_bounds__(256) factor_exp_kernel(const float* F, int d, int nch, signed char* out) {
+  const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (size_t)d * nch) return;
+  const int r = (int)(wid / nch), c = (int)(wid % nch);
+  float mx = 0.f;
+  for (int k = lane; k < CK; k += 32) {
+    const int gk = c * CK + k;
+    if (gk < d) mx = fmaxf(mx, fabsf(F[(size_t)r * d + gk]));
+  }
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) out[wid] = (signed char)bound_exp(mx);
+}
+
+// Digits of a d x d factor, once per solve:
+//   digits[((c * kDigF + a) * d + r) * CK + kk] = digit a of F[r][c*CK + kk]
+// on the (row, chunk) exponent; zero past column d.
+__global__ void __launch_bounds__(256) factor_digits_kernel(const float* F, int d, int nch, const signed char* fexp,
+                                                            __nv_bfloat16* digits) {
+  const size_t total = (size_t)d * nch * CK;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / ((size_t)nch * CK));
+    const int k = (int)(e % ((size_t)nch * CK));
+    const int c = k / CK, kk = k % CK;
+    float u = k < d ? F[(size_t)r * d + k] * pow2f(7 - (int)fexp[(size_t)r * nch + c]) : 0.f;
+#pragma unroll
+    for (int a = 0; a < kDigF; ++a) {
+      const float dg = rintf(u);
+      digits[(((size_t)c * kDigF + a) * d + r) * CK + kk] = __float2bfloat16_rn(dg);
+      u = (u - dg) * 256.f;  // exact: |u - dg| <= 1/2 and u has at most 24 significant bits
+    }
+  }
+}
+
+// Chunk product candidates closed by tile anti-diagonal K: for every column
+// J whose tile (K - J, J) closes a chunk of B tile rows, and every row I
+// whose tile (I, K - I) closes a chunk of B tile columns (candidate t:
+// columns first, J = K - (B-1) - B t, then rows likewise).  The product
+// covers the target tiles from chunk c + 2 on.
+struct ChunkCand {
+  bool col;
+  int J, I, c, first, ntiles;
+};
+__device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int ncand_col, int t, ChunkCand& cc) {
+  cc.col = t < ncand_col;
+  if (cc.col) {
+    cc.J = K - (B - 1) - B * t;
+    cc.I = 0;
+    const int last = K - cc.J;
+    if (cc.J < 0 || cc.J >= P.Nt || last >= P.Mt) return false;
+    cc.c = last / B;
+    cc.first = (cc.c + 2) * B;
+    cc.ntiles = P.Mt - cc.first;
   } else {
-    const int I = K - (B - 1) - B * (t - ncand_col);
-    const int last = K - I;
-    if (I < 0 || I >= P.Mt || last >= P.Nt) return;
-    const int c = last / B;
-    const int first = (c + 2) * B;
-    const int ntiles = P.Nt - first;
-    if (ntiles <= 0 || u * U >= ntiles) return;
-    row_push(P, sm, P.Gc, I, first + u * U, min(U, ntiles - u * U), c * B, B, sigma);
+    cc.I = K - (B - 1) - B * (t - ncand_col);
+    cc.J = 0;
+    const int last = K - cc.I;
+    if (cc.I < 0 || cc.I >= P.Mt || last >= P.Nt) return false;
+    cc.c = last / B;
+    cc.first = (cc.c + 2) * B;
+    cc.ntiles = P.Nt - cc.first;
+  }
+  return cc.ntiles > 0;
+}
+
+constexpr int kGroupsPerCta = 4;  // target groups one chunk product CTA works through
+
+struct TcSmem {
+  __nv_bfloat16 Bd[kDigD][T][CK + 8];              // source digits, [digit][q][k]
+  __nv_bfloat16 Ad[2][kDigF][UC * T][kSlab + 8];   // two k-slabs of factor digits, [buf][digit][r][k]
+  int er[kGroupsPerCta][UC * T];                   // row exponents of each group's factor block
+};
+
+__device__ __forceinline__ void ldsm_x4(unsigned& r0, unsigned& r1, unsigned& r2, unsigned& r3, const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const unsigned* a, unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Chunk products closed by tile anti-diagonal K.  blockIdx.x: candidate;
+// CTA y = blockIdx.y works through the target groups y, y + gridDim.y, ...
+// (at most kGroupsPerCta), each UC target tiles.  Column products:
+//   Xc[targets, J] += L_B[targets, chunk rows] G[chunk rows, J];
+// row products, as their transpose:
+//   Gc[I, targets]^T += L_A[targets, chunk cols] E[I, chunk cols]^T.
+// The CTA turns its source block into digits once, then streams the factor
+// digits of its groups as one sequence of k-slabs (double-buffered, the
+// next slab in flight while the current one is multiplied).
+// Warp w owns output rows 16 (w mod R) .. +15 and columns 16 (w div R) .. +15,
+// R = UC*T/16.
+__global__ void __launch_bounds__(kTcThreads, 2) chunk_tc_kernel(QParams P, int K, int ncand_col) {
+  extern __shared__ __align__(16) unsigned char tc_smem_raw[];
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(tc_smem_raw);
+  ChunkCand cc;
+  if (!chunk_candidate(P, K, ncand_col, blockIdx.x, cc)) return;
+  const int ngroups = (cc.ntiles + UC - 1) / UC;
+  const int g0 = blockIdx.y, gstep = gridDim.y;
+  if (g0 >= ngroups) return;
+  const int mygroups = min(kGroupsPerCta, (ngroups - 1 - g0) / gstep + 1);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const __nv_bfloat16* dig = cc.col ? P.digB : P.digA;
+  const signed char* fexp = cc.col ? P.expB : P.expA;
+  const int d = cc.col ? P.m : P.n;
+  const int nch = cc.col ? P.nchB : P.nchA;
+  constexpr int nslab = CK / kSlab;
+  const int nz = mygroups * nslab;  // slabs of all groups, in order
+
+  auto stage_slab = [&](int z) {
+    const int gi = z / nslab, s = z % nslab;
+    const int tr0 = cc.first + (g0 + gi * gstep) * UC;
+    const int rows = min(UC * T, (cc.first + cc.ntiles - tr0) * T);
+    const int buf = z & 1;
+    for (int e = tid; e < kDigF * UC * T * (kSlab / 8); e += kTcThreads) {
+      const int a = e / (UC * T * (kSlab / 8));
+      const int r = (e / (kSlab / 8)) % (UC * T);
+      const int k8 = 8 * (e % (kSlab / 8));
+      const int gr = tr0 * T + r;
+      const bool ok = r < rows && gr < d;
+      const __nv_bfloat16* p = dig + ((((size_t)cc.c * kDigF + a) * d + (ok ? gr : 0)) * CK + s * kSlab + k8);
+      cp_async(&sm.Ad[buf][a][r][k8], p, ok ? 16 : 0, 16);
+    }
+    cp_async_commit();
+  };
+  stage_slab(0);
+
+  // Source digits, written by the tile solves: column candidates
+  // D[k][q] = G[c*CK + k][J*T + q] from the transposed G digits, row
+  // candidates D[k][q] = E[I*T + q][c*CK + k] from the E digits; zero
+  // outside the matrix.  Rows of the digit planes start 16-byte aligned and
+  // their padding past the matrix is zero.
+  {
+    const __nv_bfloat16* dp = cc.col ? P.DGt : P.DE;
+    const size_t pst = cc.col ? P.dstrideG : P.dstrideE;
+    const int ld = cc.col ? P.ldG : P.ldE;
+    const int qlim = cc.col ? P.n : P.m, klim = cc.col ? P.m : P.n;
+    const int q0 = cc.col ? cc.J * T : cc.I * T;
+    for (int e = tid; e < kDigD * T * (CK / 8); e += kTcThreads) {
+      const int b = e / (T * (CK / 8));
+      const int q = (e / (CK / 8)) % T;
+      const int k8 = 8 * (e % (CK / 8));
+      const int gq = q0 + q, gk = cc.c * CK + k8;
+      const bool ok = gq < qlim && gk < klim;
+      const __nv_bfloat16* p = dp + (ok ? b * pst + (size_t)gq * ld + gk : 0);
+      cp_async(&sm.Bd[b][q][k8], p, ok ? 16 : 0, 16);
+    }
+  }
+  // Row exponents of every group.
+  for (int e = tid; e < mygroups * UC * T; e += kTcThreads) {
+    const int gi = e / (UC * T), r = e % (UC * T);
+    const int gr = (cc.first + (g0 + gi * gstep) * UC) * T + r;
+    sm.er[gi][r] = gr < d ? (int)fexp[(size_t)gr * nch + cc.c] : -100;
+  }
+  const int eD = bound_exp(P.hdr->sigma);
+  cp_async_commit();  // its own group; the first wait below covers it with slab 0
+  if (nz > 1) stage_slab(1);
+
+  const int rbase = 16 * (warp % kTcRowWarps), cbase = 16 * (warp / kTcRowWarps);
+  const int g = lane >> 2, tq = lane & 3;
+  float acc[kLevels][2][4];
+#pragma unroll
+  for (int l = 0; l < kLevels; ++l)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) acc[l][nt][v] = 0.f;
+
+  for (int z = 0; z < nz; ++z) {
+    const int buf = z & 1, s = z % nslab;
+    if (z + 1 < nz) {
+      cp_async_wait_all_but_one();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncthreads();  // slab z (and, at z = 0, the source digits) visible to all
+#pragma unroll
+    for (int k16 = 0; k16 < kSlab; k16 += 16) {
+      unsigned af[kDigF][4];
+#pragma unroll
+      for (int a = 0; a < kDigF; ++a)
+        ldsm_x4(af[a][0], af[a][1], af[a][2], af[a][3], &sm.Ad[buf][a][rbase + (lane & 15)][k16 + (lane >> 4) * 8]);
+      const int kg = s * kSlab + k16;
+#pragma unroll
+      for (int b = 0; b < kDigD; ++b) {
+        unsigned b0, b1, b2, b3;
+        ldsm_x4(b0, b1, b2, b3, &sm.Bd[b][cbase + (lane & 7) + ((lane >> 4) << 3)][kg + ((lane >> 3) & 1) * 8]);
+#pragma unroll
+        for (int a = 0; a < kDigF && a + b < kLevels; ++a) {
+          mma_bf16_16816(acc[a + b][0], af[a], b0, b1);
+          mma_bf16_16816(acc[a + b][1], af[a], b2, b3);
+        }
+      }
+    }
+    __syncthreads();  // buffer `buf` free
+    if (z + 2 < nz) stage_slab(z + 2);
+
+    if (s == nslab - 1) {
+      // Group done: every output in double-float (levels 0..2 exactly, each
+      // an integer sum below 2^24 on its own grid; the rest, below 2^-24 of
+      // the total, in one fp32 sum), scaled by a power of two, added to its
+      // plane.  The next slabs are already in flight.
+      const int gi = z / nslab;
+      const int tr0 = cc.first + (g0 + gi * gstep) * UC;
+      const int rows = min(UC * T, (cc.first + cc.ntiles - tr0) * T);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int r = rbase + g + 8 * (v >> 1);
+          const int q = cbase + 8 * nt + 2 * tq + (v & 1);
+          float2 y = two_sum(acc[0][nt][v], acc[1][nt][v] * 0x1p-8f);
+          const float2 y2 = two_sum(y.y, acc[2][nt][v] * 0x1p-16f);
+          const float tail = acc[3][nt][v] * 0x1p-24f + acc[4][nt][v] * 0x1p-32f + acc[5][nt][v] * 0x1p-40f;
+          y = two_sum(y.x, y2.x);  // any level may be zero: no ordering of magnitudes holds
+          y = two_sum(y.x, y.y + (y2.y + tail));
+#pragma unroll
+          for (int l = 0; l < kLevels; ++l) acc[l][nt][v] = 0.f;
+          if (r >= rows) continue;
+          const int ex = sm.er[gi][r] + eD - 14;
+          const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
+          y = make_float2(y.x * sc, y.y * sc);
+          if (cc.col) {
+            const int gr = tr0 * T + r, gc = cc.J * T + q;
+            if (gr < P.m && gc < P.n) {
+              const size_t o = (size_t)gr * P.n + gc;
+              P.Xc[o] = df_add(P.Xc[o], y);
+            }
+          } else {
+            const int gr = cc.I * T + q, gc = tr0 * T + r;
+            if (gr < P.m && gc < P.n) {
+              const size_t o = (size_t)gr * P.n + gc;
+              P.Gc[o] = df_add(P.Gc[o], y);
+            }
+          }
+        }
+    }
   }
 }
 
@@ -619,13 +920,10 @@ class LaunchClock {
 // every call.  Streams and events are driver objects, not device memory.
 // Calls that share a set serialize their side work on its streams, which
 // is correct: each call's main stream waits only on its own events' records.
-// Dynamic shared memory: a mid push CTA holds one stage, a chunk CTA two
-// (53 KB: three chunk CTAs fit in an SM's shared memory, as in its register
-// file).  Capping chunk CTAs at two per SM with unused extra space, to keep
-// room for the other kernels, was measured slower: 22.6 against 22.3 ms on a
-// 4096 x 4096 layer, 146.6 against 136.0 ms on 14336 x 4096.
+// Dynamic shared memory: a mid push CTA holds one stage; a chunk product
+// CTA the source digits and two factor slabs (102 KB: two per SM).
 constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
-constexpr int kChunkSmem = (int)sizeof(PushSmem<2>);
+constexpr int kChunkSmem = (int)sizeof(TcSmem);
 
 struct StreamSet {
   bool ready = false;
@@ -650,7 +948,7 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     if (e != cudaSuccess) return e;
     e = cudaStreamCreateWithPriority(&S.chunk, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_push_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
+    e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
     if (e != cudaSuccess) return e;
     S.ready = true;
   }
@@ -665,15 +963,44 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
 
 }  // namespace
 
-size_t quantize_workspace_bytes(int64_t m, int64_t n) {
-  const size_t plane = align_up((size_t)m * (size_t)n * sizeof(float2));
-  return sizeof(Header) + kPlanes * plane;
+// Workspace: header, the six planes, the factor exponents and digits, the
+// source digits of E and G.
+struct WsLayout {
+  size_t plane, expA, expB, digA, digB, DE, DG, dplaneE, dplaneG, total;
+  int ldE, ldG;
+};
+WsLayout ws_layout(int64_t m, int64_t n) {
+  WsLayout L;
+  const size_t nchA = (size_t)((n + CK - 1) / CK), nchB = (size_t)((m + CK - 1) / CK);
+  L.plane = align_up((size_t)m * (size_t)n * sizeof(float2));
+  size_t off = sizeof(Header) + kPlanes * L.plane;
+  L.expA = off;
+  off += align_up((size_t)n * nchA);
+  L.expB = off;
+  off += align_up((size_t)m * nchB);
+  L.digA = off;
+  off += align_up(nchA * kDigF * (size_t)n * CK * sizeof(__nv_bfloat16));
+  L.digB = off;
+  off += align_up(nchB * kDigF * (size_t)m * CK * sizeof(__nv_bfloat16));
+  L.ldE = (int)((n + 7) / 8 * 8);
+  L.ldG = (int)((m + 7) / 8 * 8);
+  L.dplaneE = align_up((size_t)m * L.ldE * sizeof(__nv_bfloat16));
+  L.dplaneG = align_up((size_t)n * L.ldG * sizeof(__nv_bfloat16));
+  L.DE = off;
+  off += kDigD * L.dplaneE;
+  L.DG = off;
+  off += kDigD * L.dplaneG;
+  L.total = off;
+  return L;
 }
+
+size_t quantize_workspace_bytes(int64_t m, int64_t n) { return ws_layout(m, n).total; }
 
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
                             int bits, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
-  const size_t plane = align_up((size_t)m * (size_t)n * sizeof(float2));
+  const WsLayout lay = ws_layout(m, n);
+  const size_t plane = lay.plane;
   char* base = static_cast<char*>(ws);
   float2* planes = reinterpret_cast<float2*>(base + sizeof(Header));
   const size_t pstride = plane / sizeof(float2);
@@ -692,6 +1019,18 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.G = planes + 4 * pstride;
   P.E = planes + 5 * pstride;
   P.status = status_dev;
+  P.expA = reinterpret_cast<const signed char*>(base + lay.expA);
+  P.expB = reinterpret_cast<const signed char*>(base + lay.expB);
+  P.digA = reinterpret_cast<const __nv_bfloat16*>(base + lay.digA);
+  P.digB = reinterpret_cast<const __nv_bfloat16*>(base + lay.digB);
+  P.DE = reinterpret_cast<__nv_bfloat16*>(base + lay.DE);
+  P.DGt = reinterpret_cast<__nv_bfloat16*>(base + lay.DG);
+  P.dstrideE = lay.dplaneE / sizeof(__nv_bfloat16);
+  P.dstrideG = lay.dplaneG / sizeof(__nv_bfloat16);
+  P.ldE = lay.ldE;
+  P.ldG = lay.ldG;
+  P.nchA = (n + CK - 1) / CK;
+  P.nchB = (m + CK - 1) / CK;
   P.m = m;
   P.n = n;
   P.Mt = (m + T - 1) / T;
@@ -723,12 +1062,27 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   err = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(P.hdr, 0, sizeof(Header), stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(planes, 0, 4 * plane, stream);  // Xm, Xc, Gm, Gc
+  // Digit rows are padded to a multiple of 8 entries; the chunk products
+  // read the padding, which must then be zero.
+  if (err == cudaSuccess && (lay.ldE != n || lay.ldG != m))
+    err = cudaMemsetAsync(base + lay.DE, 0, kDigD * (lay.dplaneE + lay.dplaneG), stream);
   if (err != cudaSuccess) return err;
   const size_t total = (size_t)m * n;
   const int pre_blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
   clock.begin(0, stream);
   prepass_kernel<<<pre_blocks, 256, 0, stream>>>(P);
   sigma_kernel<<<1, 1, 0, stream>>>(P);
+  {
+    signed char* eA = reinterpret_cast<signed char*>(base + lay.expA);
+    signed char* eB = reinterpret_cast<signed char*>(base + lay.expB);
+    __nv_bfloat16* dA = reinterpret_cast<__nv_bfloat16*>(base + lay.digA);
+    __nv_bfloat16* dB = reinterpret_cast<__nv_bfloat16*>(base + lay.digB);
+    const size_t wA = (size_t)n * P.nchA, wB = (size_t)m * P.nchB;  // one warp per (row, chunk)
+    factor_exp_kernel<<<(unsigned)((wA + 7) / 8), 256, 0, stream>>>(LA, n, P.nchA, eA);
+    factor_exp_kernel<<<(unsigned)((wB + 7) / 8), 256, 0, stream>>>(LB, m, P.nchB, eB);
+    factor_digits_kernel<<<152 * 8, 256, 0, stream>>>(LA, n, P.nchA, eA, dA);
+    factor_digits_kernel<<<152 * 8, 256, 0, stream>>>(LB, m, P.nchB, eB, dB);
+  }
   clock.end(0.0);
   cudaEventRecord(ev_start, stream);
   cudaStreamWaitEvent(s_mid, ev_start, 0);
@@ -773,19 +1127,29 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
     const int ncc = std::min(K, P.Mt - 1) >= B - 1 ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
     const int ncr = std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0;
     double chunk_tiles = 0;
+    int chunk_most = 0;  // most targets of one candidate
     for (int t = 0; t < ncc; ++t) {
       const int J = K - (B - 1) - B * t, last = K - J;
-      if (J >= 0 && J < P.Nt && last < P.Mt) chunk_tiles += std::max(0, P.Mt - (last / B + 2) * B);
+      if (J >= 0 && J < P.Nt && last < P.Mt) {
+        const int nt = std::max(0, P.Mt - (last / B + 2) * B);
+        chunk_tiles += nt;
+        chunk_most = std::max(chunk_most, nt);
+      }
     }
     for (int t = 0; t < ncr; ++t) {
       const int I = K - (B - 1) - B * t, last = K - I;
-      if (I >= 0 && I < P.Mt && last < P.Nt) chunk_tiles += std::max(0, P.Nt - (last / B + 2) * B);
+      if (I >= 0 && I < P.Mt && last < P.Nt) {
+        const int nt = std::max(0, P.Nt - (last / B + 2) * B);
+        chunk_tiles += nt;
+        chunk_most = std::max(chunk_most, nt);
+      }
     }
     if (chunk_tiles > 0) {
       cudaStreamWaitEvent(s_chunk, ev_solve[K], 0);
-      const int units = (std::max(P.Mt, P.Nt) + U - 1) / U;
+      const int groups = (chunk_most + UC - 1) / UC;
+      const int ctas = (groups + kGroupsPerCta - 1) / kGroupsPerCta;  // CTAs per candidate
       clock.begin(3, s_chunk);
-      chunk_push_kernel<<<dim3(ncc + ncr, units), 256, kChunkSmem, s_chunk>>>(P, K, ncc);
+      chunk_tc_kernel<<<dim3(ncc + ncr, ctas), kTcThreads, kChunkSmem, s_chunk>>>(P, K, ncc);
       clock.end(2.0 * B * t3 * chunk_tiles);
       cudaEventRecord(ev_chunk[K], s_chunk);
       chunk_on[K] = 1;
