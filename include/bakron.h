@@ -106,10 +106,11 @@ int bakron_prepare(const float* A, const float* B, int64_t m, int64_t n, float* 
  * numbers (about 44 significant bits), products are summed with an
  * error-free offset accumulator (Rump, Ogita and Oishi, "Accurate
  * floating-point summation, part I", 2008, ExtractScalar).  The batched
- * products run on the tensor cores through an exact split of both operands
- * into bf16 integer digits (Ozaki, Ogita, Oishi and Rump, Numer. Algorithms
- * 2012): 5 digits per factor element, 6 per double-float value, every
- * digit-pair product and every per-level sum exact in fp32.
+ * products run on the tensor cores (tcgen05, accumulators in tensor memory)
+ * through an exact split of both operands into bf16 integer digits (Ozaki,
+ * Ogita, Oishi and Rump, Numer. Algorithms 2012): 5 digits per factor
+ * element, 6 per double-float value, every digit-pair product and every
+ * per-level sum exact in fp32.
  */
 
 /* Workspace bytes bakron_quantize needs for an m x n problem. */
@@ -142,10 +143,10 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
  * (host memory) receiving, per kernel class, the summed event time in ms,
  * the number of launches and the algorithmic flops (2 per multiply-add of
  * the products L_B E L_A^T the class computes).  Classes: 0 = input
- * check and set-up (including the factors' digits), 1 = tile solve
- * (diagonal blocks and the distance-1 neighbours), 2 = mid pushes (single
- * source tiles), 3 = chunk products (batched source tiles on the tensor
- * cores, with the digits of their sources).  Synchronizes `stream` before it returns; the
+ * check and set-up (including the factors' block exponents), 1 = tile
+ * solve (diagonal blocks and the distance-1 neighbours), 2 = mid pushes
+ * (single source tiles), 3 = chunk products (batched source tiles, on the
+ * tensor cores).  Synchronizes `stream` before it returns; the
  * events add a little time to every launch.
  */
 #define BAKRON_KERNEL_CLASSES 4
@@ -182,9 +183,8 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
  * until the process exits.  The caller still passes (and owns) W, LA, LB,
  * scales, V, Wq and status_dev.  Sizes with
  * bakron_quantize_workspace_size(m, n) > BAKRON_NOALLOC_SCRATCH_BYTES
- * (72 bytes of solver state per weight plus 10 bytes per element of each
- * factor for its digits: about 92 bytes per weight for a square layer, up
- * to about 1.09 million weights, e.g. 1024 x 1024) are rejected with
+ * (72 bytes of solver state per weight: up to about 1.16 million weights,
+ * e.g. 1024 x 1024) are rejected with
  * BAKRON_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on a device looks up the array's device address for that
@@ -194,7 +194,7 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
  * behind; each call re-initializes what it reads, but calls that overlap on
  * the GPU (other streams, other host threads) race on it: serialize them.
  */
-#define BAKRON_NOALLOC_SCRATCH_BYTES ((size_t)96 << 20)
+#define BAKRON_NOALLOC_SCRATCH_BYTES ((size_t)80 << 20)
 int bakron_quantize_noalloc(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, int32_t* status_dev, void* stream);
 

@@ -39,9 +39,12 @@
 // later entry folds in the one new term of its row sum (E[p, k-p] L_A[q, k-p])
 // and of its column sum (L_B[p, k-q] Gin[k-q, q], Gin = in-tile row sum + error).
 //
-// Precision: every accumulation is double-float (df.cuh); the rounding
-// decision is the fp32 quotient fp32(W~) / s_i rounded half to even, with the
-// correctly rounded division used whenever the quotient is near a tie.
+// Precision: every accumulation is double-float (df.cuh) or exact (the
+// digit products of the chunk products on the tensor cores, see that
+// section); the rounding decision is the fp32 quotient fp32(W~) / s_i
+// rounded half to even, with the correctly rounded division used whenever
+// the quotient is near a tie.  The tile solves also write E and G as bf16
+// digit planes, the source operands of the chunk products.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -77,16 +80,14 @@ struct QParams {
   int32_t* V;
   float* Wq;
   float2* Xm;  // column pushes from single tiles (mid)
-  float2* Xc;  // column pushes from chunks
+  double* Xc;  // column pushes from chunks (fp64: updated by reductions, see chunk_tc_kernel)
   float2* Gm;  // row pushes from single tiles (mid)
-  float2* Gc;  // row pushes from chunks
+  double* Gc;  // row pushes from chunks (fp64, likewise)
   float2* G;   // full row transform of each solved entry
   float2* E;   // errors at rounding time
   Header* hdr;
   int32_t* status;
-  const __nv_bfloat16* digA;  // digits of L_A and L_B (chunk products)
-  const __nv_bfloat16* digB;
-  const signed char* expA;    // their (row, chunk) exponents
+  const signed char* expA;    // (row, chunk) exponents of L_A and L_B (chunk products)
   const signed char* expB;
   __nv_bfloat16* DE;          // digits of E, [digit][row][ldE], ldE = n rounded up to 8
   __nv_bfloat16* DGt;         // digits of G transposed, [digit][col][ldG], ldG = m rounded up to 8
@@ -225,8 +226,8 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     gf[t] = zero;
     if (va && vb) {
       const size_t o = (size_t)ra * P.n + cb;
-      c0[t] = df_add(df_add(make_float2(P.W[o], 0.f), P.Xm[o]), P.Xc[o]);
-      gf[t] = df_add(P.Gm[o], P.Gc[o]);
+      c0[t] = df_add(df_add(make_float2(P.W[o], 0.f), P.Xm[o]), df_from_double(P.Xc[o]));
+      gf[t] = df_add(P.Gm[o], df_from_double(P.Gc[o]));
     }
   }
   __syncthreads();
@@ -404,7 +405,7 @@ struct PushSmem {
 // row-major d x d factor F (rows >= rows_valid or >= d, columns >= d: zero).
 __device__ __forceinline__ void stage_factor(float (*dst)[T + 4], const float* F, int d, int r0, int rows_valid,
                                              int k0) {
-  if ((d % 4) == 0) {  // 16-byte aligned rows
+  if ((d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0) {  // 16-byte aligned rows
     for (int e = threadIdx.x; e < U * T * (T / 4); e += blockDim.x) {
       const int rr = e / (T / 4), k = 4 * (e % (T / 4));
       const int gr = r0 + rr, gk = k0 + k;
@@ -480,13 +481,18 @@ __device__ void column_push(const QParams& P, PushSmem<NS>& sm, float2* X, int J
   }
   const int gc = J * T + lane;
   if (gc >= P.n) return;
+  // Read-modify-write of the plane: all loads first, so that they are in
+  // flight together (a store between them would order each load after it).
+  float2 old[R];
 #pragma unroll
   for (int u = 0; u < R; ++u) {
     const int gr = tr0 * T + rbase + u;
-    if (rbase + u < rows && gr < P.m) {
-      const size_t o = (size_t)gr * P.n + gc;
-      X[o] = df_add(X[o], acc[u].value(sigma));
-    }
+    old[u] = (rbase + u < rows && gr < P.m) ? X[(size_t)gr * P.n + gc] : make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int u = 0; u < R; ++u) {
+    const int gr = tr0 * T + rbase + u;
+    if (rbase + u < rows && gr < P.m) X[(size_t)gr * P.n + gc] = df_add(old[u], acc[u].value(sigma));
   }
 }
 
@@ -542,20 +548,22 @@ __device__ void row_push(const QParams& P, PushSmem<NS>& sm, float2* Gp, int I, 
     }
     __syncthreads();
   }
+  // Read-modify-write of the plane: all loads first (see column_push).
+  float2 old[4][U];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int gr = I * T + p0 + u;
-    if (gr >= P.m) continue;
+  for (int u = 0; u < 4; ++u)
 #pragma unroll
     for (int v = 0; v < U; ++v) {
-      const int cc = lane + T * v;
-      const int gc = tc0 * T + cc;
-      if (cc < cols && gc < P.n) {
-        const size_t o = (size_t)gr * P.n + gc;
-        Gp[o] = df_add(Gp[o], acc[u][v].value(sigma));
-      }
+      const int gr = I * T + p0 + u, cc = lane + T * v, gc = tc0 * T + cc;
+      old[u][v] = (gr < P.m && cc < cols && gc < P.n) ? Gp[(size_t)gr * P.n + gc] : make_float2(0.f, 0.f);
     }
-  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      const int gr = I * T + p0 + u, cc = lane + T * v, gc = tc0 * T + cc;
+      if (gr < P.m && cc < cols && gc < P.n) Gp[(size_t)gr * P.n + gc] = df_add(old[u][v], acc[u][v].value(sigma));
+    }
 }
 
 // Mid pushes of the sources of tile anti-diagonal K (blockIdx.x: source
@@ -579,35 +587,36 @@ __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0)
   }
 }
 
-// ---- Chunk products on the tensor cores, by an exact digit split (after
-// Ozaki, Ogita, Oishi and Rump, "Error-free transformations of matrix
+// ---- Chunk products on the tensor cores (tcgen05), by an exact digit split
+// (after Ozaki, Ogita, Oishi and Rump, "Error-free transformations of matrix
 // multiplication by using fast routines of matrix multiplication and its
 // applications", Numer. Algorithms 2012).
 //
-// A chunk product is Y (UC*T x T) = F (UC*T x CK) * D (CK x T): F a block of a
-// factor (fp32), D a source block of G or E^T (double-float), CK = B*T.
-// With e_r bounding row r of F over the chunk (|F[r][k]| < 2^e_r) and e_q
-// bounding column q of D,
+// A chunk product is Y (128 x T) = F (128 x CK) * D (CK x T): F a block of
+// a factor (fp32, 128 target rows), D a source block of G or E^T
+// (double-float), CK = B*T.  With e_r bounding row r of F over the chunk
+// (|F[r][k]| < 2^e_r) and eD the global exponent of the source digits,
 //   F[r][k] ~ 2^(e_r-7) sum_{a<5} f_a[r][k] 256^-a,
-//   D[k][q] ~ 2^(e_q-7) sum_{b<6} d_b[k][q] 256^-b,
+//   D[k][q] ~ 2^(eD-7) sum_{b<6} d_b[k][q] 256^-b,
 // with integer digits |f_a|, |d_b| <= 128, exact in bf16.  Five digits hold
 // every factor element whose magnitude is at least 2^-16 of its row's bound
 // exactly (an fp32 significand has 24 bits) and the others to 2^-40 of the
-// bound; six digits hold a double-float to 48 bits.  (Four factor digits
-// leave an error near 1e-9 of sum |F||D| on factor rows whose entries span
-// a few binades; five leave 6e-13.)  Every digit product is exact, and per
-// level l = a + b the sum over k and over the <= 5 pairs of the level stays
-// below 5 * 128 * 128^2 < 2^24, so fp32 tensor-core accumulation of each
-// level is exact.  The 20 pairs of levels 0..5 are kept (the dropped ones
-// are below 2^-48 of row bound times column bound); the levels are summed
-// in double-float and scaled by 2^(e_r + e_q - 14).
-constexpr int CK = B * T;     // chunk depth (128)
-constexpr int kDigF = 5;      // digits of a factor element
-constexpr int kLevels = 6;    // levels 0 .. kDigD - 1
-constexpr int kSlab = 32;     // k-slab of factor digits staged at once
-constexpr int UC = 2;         // target tiles per chunk product CTA
-constexpr int kTcRowWarps = UC * T / 16;
-constexpr int kTcThreads = 2 * kTcRowWarps * 32;  // warps of 16 x 16 outputs
+// bound.  (Four factor digits leave an error near 1e-9 of sum |F||D| on
+// factor rows whose entries span a few binades; five leave 6e-13.)  Every
+// digit product is exact, and per level l = a + b the sum over k and over
+// the <= 5 pairs of the level stays below 5 * 128 * 128^2 < 2^24, so the
+// fp32 accumulation of each level in tensor memory is exact.  The 20 pairs
+// of levels 0..5 are kept (the dropped ones are below 2^-48 of row bound
+// times 2^eD); the levels are summed in double-float and scaled by
+// 2^(e_r + eD - 14).
+constexpr int CK = B * T;        // chunk depth (128)
+constexpr int kDigF = 5;         // digits of a factor element
+constexpr int kLevels = 6;       // levels 0 .. kDigD - 1
+constexpr int kTcM = 128;        // target rows per group (UC target tiles)
+constexpr int UC = kTcM / T;
+constexpr int kSlab = 32;        // k per slab of factor digits
+constexpr int kTcThreads = 12 * 32;
+constexpr int kGroupsPerCta = 8;  // target groups one chunk product CTA works through
 
 // Exponent of every (row, chunk) block of a d x d factor: out[r * nch + c]
 // bounds row r over columns [c*CK, (c+1)*CK).  One warp per block.
@@ -623,26 +632,6 @@ __global__ void __launch_bounds__(256) factor_exp_kernel(const float* F, int d, 
   }
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) out[wid] = (signed char)bound_exp(mx);
-}
-
-// Digits of a d x d factor, once per solve:
-//   digits[((c * kDigF + a) * d + r) * CK + kk] = digit a of F[r][c*CK + kk]
-// on the (row, chunk) exponent; zero past column d.
-__global__ void __launch_bounds__(256) factor_digits_kernel(const float* F, int d, int nch, const signed char* fexp,
-                                                            __nv_bfloat16* digits) {
-  const size_t total = (size_t)d * nch * CK;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
-    const int r = (int)(e / ((size_t)nch * CK));
-    const int k = (int)(e % ((size_t)nch * CK));
-    const int c = k / CK, kk = k % CK;
-    float u = k < d ? F[(size_t)r * d + k] * pow2f(7 - (int)fexp[(size_t)r * nch + c]) : 0.f;
-#pragma unroll
-    for (int a = 0; a < kDigF; ++a) {
-      const float dg = rintf(u);
-      digits[(((size_t)c * kDigF + a) * d + r) * CK + kk] = __float2bfloat16_rn(dg);
-      u = (u - dg) * 256.f;  // exact: |u - dg| <= 1/2 and u has at most 24 significant bits
-    }
-  }
 }
 
 // Chunk product candidates closed by tile anti-diagonal K: for every column
@@ -676,42 +665,113 @@ __device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int nca
   return cc.ntiles > 0;
 }
 
-constexpr int kGroupsPerCta = 4;  // target groups one chunk product CTA works through
+// -- tcgen05 building blocks.  Operands in shared memory use the canonical
+// K-major layout without swizzle: 8-row x 16-byte core matrices,
+//   offset(r, k) = (r/8) SBO + (k/8) LBO + (r%8) 16 + (k%8) 2 bytes.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Shared memory matrix descriptor: start address, leading (K) and stride
+// (M/N) byte offsets, descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(da), "l"(db), "r"(idesc), "r"(acc));
+}
+
+// Arrives on the mbarrier once every tcgen05.mma issued so far by this
+// thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(mbar))
+               : "memory");
+}
+
+// Waits for the completion of the mbarrier phase of the given parity, for
+// at most about 0.1 s (2^28 cycles; a legitimate wait here is microseconds).
+// Once a wait of this thread has run out (`broken`), later waits return at
+// once, so a CTA whose products never complete still ends promptly; the
+// caller reports BAKRON_DEV_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, bool& broken) {
+  if (broken) return false;
+  const long long t0 = clock64();
+  uint32_t done = 0;
+  while (!done) {
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done)
+                 : "r"(smem_u32(mbar)), "r"(parity)
+                 : "memory");
+    if (!done && clock64() - t0 > (1ll << 28)) {
+      broken = true;
+      return false;
+    }
+  }
+  return true;
+}
+
+// 8 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Warp roles of a chunk product CTA.
+constexpr int kTcMmaWarp = 0;           // issues the tensor-core products (lane 0)
+constexpr int kTcEpiWarp0 = 4;          // warps 4..7: epilogue, tensor-memory lane quarters 0..3
+constexpr int kTcProducers = 7 * 32;    // warps 1..3 and 8..11: factor loads and digits
+constexpr int kTcStages = 3;            // fp32 factor slabs in flight per producer
 
 struct TcSmem {
-  __nv_bfloat16 Bd[kDigD][T][CK + 8];              // source digits, [digit][q][k]
-  __nv_bfloat16 Ad[2][kDigF][UC * T][kSlab + 8];   // two k-slabs of factor digits, [buf][digit][r][k]
-  int er[kGroupsPerCta][UC * T];                   // row exponents of each group's factor block
+  __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
+  __nv_bfloat16 Bd[kDigD * T * CK];         // source digits, 192 rows (digit-major) x CK, SBO 2048 B
+  float stage[kTcStages][kTcM][kSlab];      // fp32 factor slabs as loaded
+  int er[kGroupsPerCta][kTcM];              // row exponents of each group's factor block
+  uint64_t full[2];                         // digit slab p written (producer arrivals)
+  uint64_t empty[2];                        // products reading digit slab p done (commit)
+  uint64_t grp_full[2];                     // products of a group in tensor-memory half h done (commit)
+  uint64_t grp_empty[2];                    // epilogue of tensor-memory half h done (epilogue arrivals)
+  uint32_t tmem_base;
 };
-
-__device__ __forceinline__ void ldsm_x4(unsigned& r0, unsigned& r1, unsigned& r2, unsigned& r3, const void* p) {
-  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float* c, const unsigned* a, unsigned b0, unsigned b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 // Chunk products closed by tile anti-diagonal K.  blockIdx.x: candidate;
 // CTA y = blockIdx.y works through the target groups y, y + gridDim.y, ...
-// (at most kGroupsPerCta), each UC target tiles.  Column products:
+// (at most kGroupsPerCta), each 128 target rows.  Column products:
 //   Xc[targets, J] += L_B[targets, chunk rows] G[chunk rows, J];
 // row products, as their transpose:
 //   Gc[I, targets]^T += L_A[targets, chunk cols] E[I, chunk cols]^T.
-// The CTA turns its source block into digits once, then streams the factor
-// digits of its groups as one sequence of k-slabs (double-buffered, the
-// next slab in flight while the current one is multiplied).
-// Warp w owns output rows 16 (w mod R) .. +15 and columns 16 (w div R) .. +15,
-// R = UC*T/16.
-__global__ void __launch_bounds__(kTcThreads, 2) chunk_tc_kernel(QParams P, int K, int ncand_col) {
-  extern __shared__ __align__(16) unsigned char tc_smem_raw[];
+// Warp-specialized pipeline over the k-slabs of all groups of the CTA:
+//  * producers copy fp32 factor slabs two ahead (cp.async, each thread its
+//    own items) and turn them into digits in one of two digit buffers, once
+//    the products that read that buffer are done;
+//  * one thread issues, per 16-deep k-step, five MMAs: factor digit a times
+//    the source digits 0 .. 5-a stacked along N (N = 32 (6 - a)), written at
+//    tensor-memory column 32 a, so the block of source digit b lands on
+//    level a + b: the 20 digit pairs in five products;
+//  * epilogue warps turn each finished group's six levels into double-float
+//    updates of the plane, while the next group is multiplied in the other
+//    tensor-memory half.
+// Handshakes are mbarriers; every wait is bounded.
+// (At most 80 registers: 30 K registers, so that a tile solve fits beside
+// it; its shared memory admits one per SM.)
+__global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col) {
+  extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>(tc_smem_raw);
   ChunkCand cc;
   if (!chunk_candidate(P, K, ncand_col, blockIdx.x, cc)) return;
@@ -720,142 +780,206 @@ __global__ void __launch_bounds__(kTcThreads, 2) chunk_tc_kernel(QParams P, int 
   if (g0 >= ngroups) return;
   const int mygroups = min(kGroupsPerCta, (ngroups - 1 - g0) / gstep + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const __nv_bfloat16* dig = cc.col ? P.digB : P.digA;
+  const bool is_epi = warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4;
+  const bool is_prod = warp != kTcMmaWarp && !is_epi;
+  const int ptid = is_prod ? (warp < kTcEpiWarp0 ? tid - 32 : tid - 160) : -1;  // 0 .. kTcProducers-1
+  static_assert(kTcThreads == 12 * 32 && kTcProducers == 7 * 32, "warp roles: 1 + 4 + 7");
+  const float* F = cc.col ? P.LB : P.LA;
   const signed char* fexp = cc.col ? P.expB : P.expA;
   const int d = cc.col ? P.m : P.n;
   const int nch = cc.col ? P.nchB : P.nchA;
   constexpr int nslab = CK / kSlab;
   const int nz = mygroups * nslab;  // slabs of all groups, in order
+  const bool vec4 = (d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0;
+  auto group_row0 = [&](int gi) { return (cc.first + (g0 + gi * gstep) * UC) * T; };
+  auto group_rows = [&](int gi) { return min(kTcM, (cc.first + cc.ntiles) * T - group_row0(gi)); };
 
-  auto stage_slab = [&](int z) {
-    const int gi = z / nslab, s = z % nslab;
-    const int tr0 = cc.first + (g0 + gi * gstep) * UC;
-    const int rows = min(UC * T, (cc.first + cc.ntiles - tr0) * T);
-    const int buf = z & 1;
-    for (int e = tid; e < kDigF * UC * T * (kSlab / 8); e += kTcThreads) {
-      const int a = e / (UC * T * (kSlab / 8));
-      const int r = (e / (kSlab / 8)) % (UC * T);
-      const int k8 = 8 * (e % (kSlab / 8));
-      const int gr = tr0 * T + r;
-      const bool ok = r < rows && gr < d;
-      const __nv_bfloat16* p = dig + ((((size_t)cc.c * kDigF + a) * d + (ok ? gr : 0)) * CK + s * kSlab + k8);
-      cp_async(&sm.Ad[buf][a][r][k8], p, ok ? 16 : 0, 16);
+  // Producer item it (of kTcM * kSlab / 8): row it / 4, columns 8 (it mod 4) .. +7.
+  auto copy_slab = [&](int z) {
+    if (z < nz) {
+      const int gi = z / nslab, s = z % nslab;
+      const int row0 = group_row0(gi), rows = group_rows(gi);
+      for (int it = ptid; it < kTcM * kSlab / 8; it += kTcProducers) {
+        const int r = it / 4, k8 = 8 * (it % 4);
+        const int gr = row0 + r, gk = cc.c * CK + s * kSlab + k8;
+        const bool rok = r < rows && gr < d;
+        float* dst = &sm.stage[z % kTcStages][r][k8];
+        const float* src = F + (size_t)(rok ? gr : 0) * d;
+        if (vec4) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const bool ok = rok && gk + 4 * h < d;
+            cp_async(dst + 4 * h, ok ? (const void*)(src + gk + 4 * h) : (const void*)F, ok ? 16 : 0, 16);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool ok = rok && gk + e < d;
+            cp_async(dst + e, ok ? (const void*)(src + gk + e) : (const void*)F, ok ? 4 : 0, 4);
+          }
+        }
+      }
     }
-    cp_async_commit();
+    cp_async_commit();  // one group per slab, empty past the end, so that the counts stay uniform
   };
-  stage_slab(0);
 
-  // Source digits, written by the tile solves: column candidates
-  // D[k][q] = G[c*CK + k][J*T + q] from the transposed G digits, row
-  // candidates D[k][q] = E[I*T + q][c*CK + k] from the E digits; zero
-  // outside the matrix.  Rows of the digit planes start 16-byte aligned and
-  // their padding past the matrix is zero.
-  {
+  // Prologue: source digits (written by the tile solves) with all producer
+  // threads, row exponents, mbarriers, tensor memory; the first two slabs.
+  if (is_prod) {
     const __nv_bfloat16* dp = cc.col ? P.DGt : P.DE;
     const size_t pst = cc.col ? P.dstrideG : P.dstrideE;
     const int ld = cc.col ? P.ldG : P.ldE;
     const int qlim = cc.col ? P.n : P.m, klim = cc.col ? P.m : P.n;
     const int q0 = cc.col ? cc.J * T : cc.I * T;
-    for (int e = tid; e < kDigD * T * (CK / 8); e += kTcThreads) {
+    for (int e = ptid; e < kDigD * T * (CK / 8); e += kTcProducers) {
       const int b = e / (T * (CK / 8));
       const int q = (e / (CK / 8)) % T;
       const int k8 = 8 * (e % (CK / 8));
       const int gq = q0 + q, gk = cc.c * CK + k8;
       const bool ok = gq < qlim && gk < klim;
       const __nv_bfloat16* p = dp + (ok ? b * pst + (size_t)gq * ld + gk : 0);
-      cp_async(&sm.Bd[b][q][k8], p, ok ? 16 : 0, 16);
+      const int row = b * T + q;  // stacked digit-major
+      unsigned char* dst = reinterpret_cast<unsigned char*>(sm.Bd) + (row / 8) * 2048 + (k8 / 8) * 128 + (row % 8) * 16;
+      cp_async(dst, p, ok ? 16 : 0, 16);
     }
+    cp_async_commit();
+    copy_slab(0);
+    copy_slab(1);
   }
-  // Row exponents of every group.
-  for (int e = tid; e < mygroups * UC * T; e += kTcThreads) {
-    const int gi = e / (UC * T), r = e % (UC * T);
-    const int gr = (cc.first + (g0 + gi * gstep) * UC) * T + r;
+  for (int e = tid; e < mygroups * kTcM; e += blockDim.x) {
+    const int gi = e / kTcM, r = e % kTcM;
+    const int gr = group_row0(gi) + r;
     sm.er[gi][r] = gr < d ? (int)fexp[(size_t)gr * nch + cc.c] : -100;
   }
-  const int eD = bound_exp(P.hdr->sigma);
-  cp_async_commit();  // its own group; the first wait below covers it with slab 0
-  if (nz > 1) stage_slab(1);
-
-  const int rbase = 16 * (warp % kTcRowWarps), cbase = 16 * (warp / kTcRowWarps);
-  const int g = lane >> 2, tq = lane & 3;
-  float acc[kLevels][2][4];
+  if (tid == 0) {
 #pragma unroll
-  for (int l = 0; l < kLevels; ++l)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int v = 0; v < 4; ++v) acc[l][nt][v] = 0.f;
-
-  for (int z = 0; z < nz; ++z) {
-    const int buf = z & 1, s = z % nslab;
-    if (z + 1 < nz) {
-      cp_async_wait_all_but_one();
-    } else {
-      cp_async_wait_all();
-    }
-    __syncthreads();  // slab z (and, at z = 0, the source digits) visible to all
-#pragma unroll
-    for (int k16 = 0; k16 < kSlab; k16 += 16) {
-      unsigned af[kDigF][4];
-#pragma unroll
-      for (int a = 0; a < kDigF; ++a)
-        ldsm_x4(af[a][0], af[a][1], af[a][2], af[a][3], &sm.Ad[buf][a][rbase + (lane & 15)][k16 + (lane >> 4) * 8]);
-      const int kg = s * kSlab + k16;
-#pragma unroll
-      for (int b = 0; b < kDigD; ++b) {
-        unsigned b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, &sm.Bd[b][cbase + (lane & 7) + ((lane >> 4) << 3)][kg + ((lane >> 3) & 1) * 8]);
-#pragma unroll
-        for (int a = 0; a < kDigF && a + b < kLevels; ++a) {
-          mma_bf16_16816(acc[a + b][0], af[a], b0, b1);
-          mma_bf16_16816(acc[a + b][1], af[a], b2, b3);
-        }
-      }
-    }
-    __syncthreads();  // buffer `buf` free
-    if (z + 2 < nz) stage_slab(z + 2);
-
-    if (s == nslab - 1) {
-      // Group done: every output in double-float (levels 0..2 exactly, each
-      // an integer sum below 2^24 on its own grid; the rest, below 2^-24 of
-      // the total, in one fp32 sum), scaled by a power of two, added to its
-      // plane.  The next slabs are already in flight.
-      const int gi = z / nslab;
-      const int tr0 = cc.first + (g0 + gi * gstep) * UC;
-      const int rows = min(UC * T, (cc.first + cc.ntiles - tr0) * T);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int r = rbase + g + 8 * (v >> 1);
-          const int q = cbase + 8 * nt + 2 * tq + (v & 1);
-          float2 y = two_sum(acc[0][nt][v], acc[1][nt][v] * 0x1p-8f);
-          const float2 y2 = two_sum(y.y, acc[2][nt][v] * 0x1p-16f);
-          const float tail = acc[3][nt][v] * 0x1p-24f + acc[4][nt][v] * 0x1p-32f + acc[5][nt][v] * 0x1p-40f;
-          y = two_sum(y.x, y2.x);  // any level may be zero: no ordering of magnitudes holds
-          y = two_sum(y.x, y.y + (y2.y + tail));
-#pragma unroll
-          for (int l = 0; l < kLevels; ++l) acc[l][nt][v] = 0.f;
-          if (r >= rows) continue;
-          const int ex = sm.er[gi][r] + eD - 14;
-          const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
-          y = make_float2(y.x * sc, y.y * sc);
-          if (cc.col) {
-            const int gr = tr0 * T + r, gc = cc.J * T + q;
-            if (gr < P.m && gc < P.n) {
-              const size_t o = (size_t)gr * P.n + gc;
-              P.Xc[o] = df_add(P.Xc[o], y);
-            }
-          } else {
-            const int gr = cc.I * T + q, gc = tr0 * T + r;
-            if (gr < P.m && gc < P.n) {
-              const size_t o = (size_t)gr * P.n + gc;
-              P.Gc[o] = df_add(P.Gc[o], y);
-            }
-          }
-        }
+    for (int i = 0; i < 2; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])), "r"(kTcProducers));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.grp_full[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.grp_empty[i])));
     }
   }
+  if (warp == kTcMmaWarp) {  // two tensor-memory halves of 256 columns (6 levels x 32 used in each)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(&sm.tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  if (is_prod) {
+    asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // the source digits (slabs 0, 1 may be in flight)
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int eD = bound_exp(P.hdr->sigma);
+  bool broken = false;
+
+  if (is_prod) {
+    for (int z = 0; z < nz; ++z) {
+      const int p = z & 1, gi = z / nslab;
+      copy_slab(z + 2);
+      asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // this thread's items of slab z
+      if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+      for (int it = ptid; it < kTcM * kSlab / 8; it += kTcProducers) {
+        const int r = it / 4, k8 = 8 * (it % 4);
+        const float sc = pow2f(7 - sm.er[gi][r]);
+        const float4 x0 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8]);
+        const float4 x1 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8 + 4]);
+        float u[8] = {x0.x * sc, x0.y * sc, x0.z * sc, x0.w * sc, x1.x * sc, x1.y * sc, x1.z * sc, x1.w * sc};
+        const int off = (r / 8) * 512 + (k8 / 8) * 128 + (r % 8) * 16;
+#pragma unroll
+        for (int a = 0; a < kDigF; ++a) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float d0 = rintf(u[2 * e]), d1 = rintf(u[2 * e + 1]);
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);  // low half: the smaller k
+            w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+            u[2 * e] = (u[2 * e] - d0) * 256.f;  // exact: |u - d| <= 1/2, u has <= 24 significant bits
+            u[2 * e + 1] = (u[2 * e + 1] - d1) * 256.f;
+          }
+          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(sm.A[p][a]) + off) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[p])) : "memory");
+    }
+  } else if (warp == kTcMmaWarp) {
+    if (lane == 0) {
+      for (int z = 0; z < nz; ++z) {
+        const int p = z & 1, gi = z / nslab, s = z % nslab, h = gi & 1;
+        if (s == 0 && gi >= 2) mbar_wait(&sm.grp_empty[h], (uint32_t)((gi >> 1) - 1) & 1u, broken);
+        mbar_wait(&sm.full[p], (uint32_t)(z >> 1) & 1u, broken);
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < kSlab / 16; ++j) {
+          const uint64_t db = umma_sdesc(smem_u32(sm.Bd) + (uint32_t)((s * kSlab + 16 * j) / 8) * 128u, 128u, 2048u);
+#pragma unroll
+          for (int a = 0; a < kDigF; ++a) {
+            const uint64_t da = umma_sdesc(smem_u32(sm.A[p][a]) + (uint32_t)(2 * j) * 128u, 128u, 512u);
+            const uint32_t acc = (s > 0 || j > 0 || a > 0) ? 1u : 0u;
+            umma_bf16(tmem + (uint32_t)(256 * h + 32 * a), da, db, umma_idesc_bf16(kTcM, T * (kDigD - a)), acc);
+          }
+        }
+        umma_commit(&sm.empty[p]);
+        if (s == nslab - 1) umma_commit(&sm.grp_full[h]);
+      }
+    }
+    __syncwarp();
+  } else {  // epilogue warps
+    const int qd = warp - kTcEpiWarp0;  // tensor-memory lane quarter
+    const int r = 32 * qd + lane;       // output row of this thread within the group
+    for (int gi = 0; gi < mygroups; ++gi) {
+      const int h = gi & 1;
+      mbar_wait(&sm.grp_full[h], (uint32_t)(gi >> 1) & 1u, broken);
+      tc_fence_after();
+      const int row0 = group_row0(gi), rows = group_rows(gi);
+      const int ex = sm.er[gi][r] + eD - 14;
+      const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
+      // Output (row r, column q) of the group: column products update
+      // Xc[row0 + r][J*T + q], row products Gc[I*T + q][row0 + r].  The two
+      // chunk planes are fp64 and take each update as a reduction in L2
+      // (red.global.add.f64: no load, no wait).  A double-float value of at
+      // most 48 significant bits converts to fp64 exactly; an element gets at
+      // most one update per launch, so with one chunk stream its fp64
+      // additions (each rounded to 53 bits) come in a fixed order.
+      double* plane = cc.col ? P.Xc : P.Gc;
+      const int gr0 = cc.col ? row0 + r : cc.I * T, gc0 = cc.col ? cc.J * T : row0 + r;
+      const bool rok = r < rows && (cc.col ? gr0 < P.m : gc0 < P.n);
+      const size_t obase = rok ? (size_t)gr0 * P.n + gc0 : 0;
+      const size_t ostep = cc.col ? 1 : (size_t)P.n;  // next q
+      const int qlim = cc.col ? P.n - gc0 : P.m - gr0;
+#pragma unroll 1
+      for (int qb = 0; qb < T; qb += 8) {
+        float lv[kLevels][8];
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)
+          tmem_ld8(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + 32 * l + qb), lv[l]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          // levels 0..2 exactly (each an integer sum below 2^24 on its own
+          // grid), the rest (below 2^-24 of the total) in one fp32 sum
+          float2 y = two_sum(lv[0][j], lv[1][j] * 0x1p-8f);
+          const float2 y2 = two_sum(y.y, lv[2][j] * 0x1p-16f);
+          const float tail = lv[3][j] * 0x1p-24f + lv[4][j] * 0x1p-32f + lv[5][j] * 0x1p-40f;
+          y = two_sum(y.x, y2.x);  // any level may be zero: no ordering of magnitudes holds
+          y = two_sum(y.x, y.y + (y2.y + tail));
+          if (rok && qb + j < qlim)
+            atomicAdd(plane + obase + (size_t)(qb + j) * ostep, ((double)y.x + (double)y.y) * (double)sc);
+        }
+      }
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.grp_empty[h])) : "memory");
+    }
+  }
+  if (broken) atomicOr(P.status, BAKRON_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));
 }
 
 // Event pairs around launches when a KernelTimer is given (diagnostics).
@@ -916,18 +1040,27 @@ class LaunchClock {
   std::vector<Rec> recs_;
 };
 
-// Two side streams and the ordering events, one set per device, reused by
-// every call.  Streams and events are driver objects, not device memory.
+// The side streams (mid pushes; chunk products) and the ordering events,
+// one set per device, reused by every call.  Streams and events are driver objects, not device memory.
 // Calls that share a set serialize their side work on its streams, which
 // is correct: each call's main stream waits only on its own events' records.
 // Dynamic shared memory: a mid push CTA holds one stage; a chunk product
-// CTA the source digits and two factor slabs (102 KB: two per SM).
+// CTA the source digits, two factor digit slabs and three fp32 factor slabs
+// (178 KB: one per SM, with room beside it for a tile solve).
 constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
 constexpr int kChunkSmem = (int)sizeof(TcSmem);
 
+// Chunk launches of consecutive tile anti-diagonals go round-robin over
+// kChunkStreams streams.  With more than one they overlap and may update
+// the same plane elements, which the fp64 reductions make safe but whose
+// order then varies from run to run; one stream (the default: more were not
+// faster, 19.0 against 19.3 ms on a 4096 x 4096 layer, 95.4 against 91.4 ms
+// on 14336 x 4096) keeps every sum in a fixed order.
+constexpr int kChunkStreams = 1;
+
 struct StreamSet {
   bool ready = false;
-  cudaStream_t mid = nullptr, chunk = nullptr;
+  cudaStream_t mid = nullptr, chunk[kChunkStreams] = {};
   std::vector<cudaEvent_t> ev;
 };
 constexpr int kMaxDevices = 128;
@@ -946,8 +1079,10 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     (void)lo;
     e = cudaStreamCreateWithPriority(&S.mid, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
-    e = cudaStreamCreateWithPriority(&S.chunk, cudaStreamNonBlocking, hi);
-    if (e != cudaSuccess) return e;
+    for (int i = 0; i < kChunkStreams; ++i) {
+      e = cudaStreamCreateWithPriority(&S.chunk[i], cudaStreamNonBlocking, hi);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
     if (e != cudaSuccess) return e;
     S.ready = true;
@@ -963,10 +1098,10 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
 
 }  // namespace
 
-// Workspace: header, the six planes, the factor exponents and digits, the
-// source digits of E and G.
+// Workspace: header, the six planes, the factor exponents, the source
+// digits of E and G.
 struct WsLayout {
-  size_t plane, expA, expB, digA, digB, DE, DG, dplaneE, dplaneG, total;
+  size_t plane, expA, expB, DE, DG, dplaneE, dplaneG, total;
   int ldE, ldG;
 };
 WsLayout ws_layout(int64_t m, int64_t n) {
@@ -978,10 +1113,6 @@ WsLayout ws_layout(int64_t m, int64_t n) {
   off += align_up((size_t)n * nchA);
   L.expB = off;
   off += align_up((size_t)m * nchB);
-  L.digA = off;
-  off += align_up(nchA * kDigF * (size_t)n * CK * sizeof(__nv_bfloat16));
-  L.digB = off;
-  off += align_up(nchB * kDigF * (size_t)m * CK * sizeof(__nv_bfloat16));
   L.ldE = (int)((n + 7) / 8 * 8);
   L.ldG = (int)((m + 7) / 8 * 8);
   L.dplaneE = align_up((size_t)m * L.ldE * sizeof(__nv_bfloat16));
@@ -1013,16 +1144,14 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.Wq = Wq;
   P.hdr = reinterpret_cast<Header*>(base);
   P.Xm = planes;
-  P.Xc = planes + pstride;
+  P.Xc = reinterpret_cast<double*>(planes + pstride);
   P.Gm = planes + 2 * pstride;
-  P.Gc = planes + 3 * pstride;
+  P.Gc = reinterpret_cast<double*>(planes + 3 * pstride);
   P.G = planes + 4 * pstride;
   P.E = planes + 5 * pstride;
   P.status = status_dev;
   P.expA = reinterpret_cast<const signed char*>(base + lay.expA);
   P.expB = reinterpret_cast<const signed char*>(base + lay.expB);
-  P.digA = reinterpret_cast<const __nv_bfloat16*>(base + lay.digA);
-  P.digB = reinterpret_cast<const __nv_bfloat16*>(base + lay.digB);
   P.DE = reinterpret_cast<__nv_bfloat16*>(base + lay.DE);
   P.DGt = reinterpret_cast<__nv_bfloat16*>(base + lay.DG);
   P.dstrideE = lay.dplaneE / sizeof(__nv_bfloat16);
@@ -1056,7 +1185,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   // With a timer every kernel runs on the caller's stream, one after the
   // other, so that each event pair brackets one kernel alone.
   cudaStream_t s_mid = timer ? stream : S.mid;
-  cudaStream_t s_chunk = timer ? stream : S.chunk;
+  auto s_chunk = [&](int K) { return timer ? stream : S.chunk[K % kChunkStreams]; };
 
   LaunchClock clock(timer);
   err = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
@@ -1075,30 +1204,29 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   {
     signed char* eA = reinterpret_cast<signed char*>(base + lay.expA);
     signed char* eB = reinterpret_cast<signed char*>(base + lay.expB);
-    __nv_bfloat16* dA = reinterpret_cast<__nv_bfloat16*>(base + lay.digA);
-    __nv_bfloat16* dB = reinterpret_cast<__nv_bfloat16*>(base + lay.digB);
     const size_t wA = (size_t)n * P.nchA, wB = (size_t)m * P.nchB;  // one warp per (row, chunk)
     factor_exp_kernel<<<(unsigned)((wA + 7) / 8), 256, 0, stream>>>(LA, n, P.nchA, eA);
     factor_exp_kernel<<<(unsigned)((wB + 7) / 8), 256, 0, stream>>>(LB, m, P.nchB, eB);
-    factor_digits_kernel<<<152 * 8, 256, 0, stream>>>(LA, n, P.nchA, eA, dA);
-    factor_digits_kernel<<<152 * 8, 256, 0, stream>>>(LB, m, P.nchB, eB, dB);
   }
   clock.end(0.0);
   cudaEventRecord(ev_start, stream);
   cudaStreamWaitEvent(s_mid, ev_start, 0);
-  cudaStreamWaitEvent(s_chunk, ev_start, 0);
+  for (int i = 0; i < kChunkStreams; ++i) cudaStreamWaitEvent(s_chunk(i), ev_start, 0);
 
   const double t3 = (double)T * T * T;
   std::vector<char> mid_on(Kmax + 1, 0), chunk_on(Kmax + 1, 0);
-  int last_mid = -1, last_chunk = -1;
+  int last_mid = -1;
+  int last_chunk[kChunkStreams];
+  for (int i = 0; i < kChunkStreams; ++i) last_chunk[i] = -1;
   for (int K = 0; K <= Kmax; ++K) {
     const int I0 = std::max(0, K - (P.Nt - 1));
     const int I1 = std::min(K, P.Mt - 1);
     const int nsrc = I1 - I0 + 1;
     if (K >= 2 && mid_on[K - 2]) cudaStreamWaitEvent(stream, ev_mid[K - 2], 0);
-    // Stream order makes one wait enough: mid(K-2) and chunk(K-B-1) follow
-    // every earlier launch of their streams, and a missing launch was covered
-    // by the wait of an earlier solve.
+    // One wait each is enough: mid(K-2) follows every earlier mid launch on
+    // its stream, every chunk launch before chunk(K-B-1) was waited for by an
+    // earlier solve (the solves are in order on one stream), and a missing
+    // launch was covered by the wait of an earlier solve.
     if (K >= B + 1 && chunk_on[K - B - 1]) cudaStreamWaitEvent(stream, ev_chunk[K - B - 1], 0);
     clock.begin(1, stream);
     tile_solve_kernel<<<nsrc, kSolveThreads, 0, stream>>>(P, K, I0);
@@ -1145,20 +1273,21 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
       }
     }
     if (chunk_tiles > 0) {
-      cudaStreamWaitEvent(s_chunk, ev_solve[K], 0);
+      cudaStreamWaitEvent(s_chunk(K), ev_solve[K], 0);
       const int groups = (chunk_most + UC - 1) / UC;
       const int ctas = (groups + kGroupsPerCta - 1) / kGroupsPerCta;  // CTAs per candidate
-      clock.begin(3, s_chunk);
-      chunk_tc_kernel<<<dim3(ncc + ncr, ctas), kTcThreads, kChunkSmem, s_chunk>>>(P, K, ncc);
+      clock.begin(3, s_chunk(K));
+      chunk_tc_kernel<<<dim3(ncc + ncr, ctas), kTcThreads, kChunkSmem, s_chunk(K)>>>(P, K, ncc);
       clock.end(2.0 * B * t3 * chunk_tiles);
-      cudaEventRecord(ev_chunk[K], s_chunk);
+      cudaEventRecord(ev_chunk[K], s_chunk(K));
       chunk_on[K] = 1;
-      last_chunk = K;
+      last_chunk[K % kChunkStreams] = K;
     }
   }
   // Join: the caller's stream covers all side work of this call.
   if (last_mid >= 0) cudaStreamWaitEvent(stream, ev_mid[last_mid], 0);
-  if (last_chunk >= 0) cudaStreamWaitEvent(stream, ev_chunk[last_chunk], 0);
+  for (int i = 0; i < kChunkStreams; ++i)
+    if (last_chunk[i] >= 0) cudaStreamWaitEvent(stream, ev_chunk[last_chunk[i]], 0);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   return clock.finish(stream);

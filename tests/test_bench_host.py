@@ -102,3 +102,15 @@ def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     with open(tmp_path / bench.KERNEL_SOURCES[0], "a") as f:
         f.write("\n// edited\n")
     assert bench.profiled_traffic("chunk_push", "c3") is None  # stale once the kernel changes
+
+
+def test_roofline_tensor_and_alu_classes():
+    import bench
+
+    peaks = {"bf16_tflops": 2000.0, "sm_max_mhz": 2000.0}
+    r = bench.roofline_for("chunk_push", 1e12, 100.0, peaks)  # 10 TFLOP/s of fp64-equivalent products
+    assert r["bound"] == "tensor" and abs(r["achieved"] - 200.0) < 1e-9 and abs(r["frac"] - 0.1) < 1e-12
+    assert abs(r["alg_tflops_fp64_equiv"] - 10.0) < 1e-12 and r["peak_basis"].startswith("measured")
+    assert bench.roofline_for("chunk_push", 1e12, 100.0, {})["peak_basis"].startswith("fallback")
+    a = bench.roofline_for("tile_solve", 1e12, 100.0, peaks)
+    assert a["bound"] == "alu" and abs(a["peak"] - bench.alu_peak_tflops(2000.0)) < 1e-12
