@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   __shared__ float sLA[T][T + 2];   // L_A[J, J]
   __shared__ float sLBo[T][T + 1];  // L_B[I, I-1]
   __shared__ float sLAo[T][T + 1];  // L_A[J, J-1]
-  __shared__ float2 sA[T][T + 2];   // G[I-1, J]; later the in-tile row sums
+  __shared__ float2 sA[T][T + 2];   // G[I-1, J]; later the in-tile row transforms Gin
   __shared__ float2 sB[T][T + 2];   // E[I, J-1]; later W0 + X; later the tile's errors
   __shared__ float2 sGx[T][T + 1];  // full row-external sum of every entry
   const float sigma = P.hdr->sigma;
@@ -250,9 +250,10 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   }
   __syncthreads();
 
-  // Skewed mapping.  acc: the whole value to round (tile input plus every
-  // in-tile term); racc: the in-tile row terms alone (needed for the row
-  // transform Gin = racc + e).
+  // Skewed mapping.  acc: the tile input and the in-tile column terms;
+  // racc: the in-tile row terms (also needed alone, for the row transform
+  // Gin = racc + e).  Both offset accumulators share sigma, so the value to
+  // round is formed from them exactly when the entry's turn comes.
   const int p = lane;
   const int r = I * T + p;
   const bool vr = r < P.m;
@@ -306,20 +307,14 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
         const bool rounds_now = (p + q == k);
         if (rounds_now != (pass == 0)) continue;
         if (p + q > ks && ks >= 0) {
-          if (jj >= 0 && jj < q) {
-            const float l = sLA[q][jj];
-            acc[j].mac(l, et);
-            racc[j].mac(l, et);
-          }
+          if (jj >= 0 && jj < q) racc[j].mac(sLA[q][jj], et);                 // row term E[p, jj] L_A[q, jj]
           const int i = ks - q;
-          if (i >= 0 && i < p) {  // column term L_B[p, i] Gin[i, q], Gin = row sum + error
-            const float l = sLB[p][i];
-            acc[j].mac(l, sA[i][q]);
-            acc[j].mac(l, sB[i][q]);
-          }
+          if (i >= 0 && i < p) acc[j].mac(sLB[p][i], sA[i][q]);                 // column term L_B[p, i] Gin[i, q]
         }
         if (rounds_now && vr && J * T + q < P.n) {
-          const float2 x = acc[j].value(sigma);
+          // (acc.H - sigma) and (racc.H - sigma) are exact and so is their
+          // sum (two multiples of the offset's half-ulp, below sigma).
+          const float2 x = two_sum((acc[j].H - sigma) + (racc[j].H - sigma), acc[j].L + racc[j].L);
           // fp32 decision: x.x == fp32(x); x.x * rcp is within 2 ulp of the
           // correctly rounded quotient, which is used near a rounding tie.
           float y = x.x * rcp;
@@ -331,7 +326,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
           const float2 h = two_sum(sv.x, -x.x);
           const float2 e = fast_two_sum(h.x, (sv.y - x.y) + h.y);
           sB[p][q] = e;
-          sA[p][q] = racc[j].value(sigma);
+          sA[p][q] = df_add(racc[j].value(sigma), e);  // Gin: the entry's in-tile row transform
           vkeep[j] = v;
         }
       }
@@ -355,7 +350,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     const int a = warp + kRows * t;
     const int ra = I * T + a;
     const float2 e = sB[a][b];
-    gv[t] = df_add(sGx[a][b], df_add(sA[a][b], e));
+    gv[t] = df_add(sGx[a][b], sA[a][b]);  // G = row-external sum + Gin
     if (ra < P.m && vb) {
       const size_t o = (size_t)ra * P.n + cb;
       P.E[o] = e;
