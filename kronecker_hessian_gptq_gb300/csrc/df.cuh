@@ -83,13 +83,6 @@ __device__ __forceinline__ float2 df_div(float2 a, float2 b) {
 }
 
 // Offset accumulator: value = (H - sigma) + L.
-// Nearest double-float to an fp64 value: hi = fp32(x), lo = fp32(x - hi)
-// (x - hi is exact in fp64).
-__device__ __forceinline__ float2 df_from_double(double x) {
-  const float hi = __double2float_rn(x);
-  return make_float2(hi, __double2float_rn(x - (double)hi));
-}
-
 struct OffsetAcc {
   float H, L;
 

@@ -80,9 +80,9 @@ struct QParams {
   int32_t* V;
   float* Wq;
   float2* Xm;  // column pushes from single tiles (mid)
-  double* Xc;  // column pushes from chunks (fp64: updated by reductions, see chunk_tc_kernel)
+  long long* Xc;  // column pushes from chunks (64-bit fixed point, see fixed_unit_exp)
   float2* Gm;  // row pushes from single tiles (mid)
-  double* Gc;  // row pushes from chunks (fp64, likewise)
+  long long* Gc;  // row pushes from chunks (likewise)
   float2* G;   // full row transform of each solved entry
   float2* E;   // errors at rounding time
   Header* hdr;
@@ -174,6 +174,31 @@ __device__ __forceinline__ void put_digits(__nv_bfloat16* planes, size_t pstride
   }
 }
 
+// The two chunk planes (Xc, Gc) hold 64-bit two's-complement fixed point in
+// units of 2^(eDc - 54), eDc = max(eD, -60) (2^eD = 2 sigma): 2^-53 sigma, 32
+// times finer than double-float, with range 2^63 units = 1024 sigma (every
+// value the solve holds is below sigma; partial sums of the chunk products
+// would have to exceed the final values a thousandfold to wrap).  The chunk
+// products add into them with integer reductions in L2 (exact, so the sums
+// do not depend on their order), and no fp64 arithmetic is needed anywhere
+// (GB300's fp64 rate is 1/64 of its fp32 rate).
+__device__ __forceinline__ int fixed_unit_exp(float sigma) { return max(bound_exp(sigma), -60) - 54; }
+
+// Double-float value x * 2^-unit_exp (|x| * 2^-unit_exp < 2^63) rounded to the
+// fixed-point grid.
+__device__ __forceinline__ long long df_to_fixed(float2 x, float to_units) {
+  return __float2ll_rn(x.x * to_units) + __float2ll_rn(x.y * to_units);
+}
+
+// Nearest double-float to a fixed-point value v * 2^unit_exp: hi is the
+// nearest float to v (an integer when |v| >= 2^24), the remainder v - hi is
+// exact in 64 bits and rounded once more for lo.
+__device__ __forceinline__ float2 df_from_fixed(long long v, float from_units) {
+  const float hi = __ll2float_rn(v);
+  const float lo = __ll2float_rn(v - __float2ll_rn(hi));
+  return make_float2(hi * from_units, lo * from_units);
+}
+
 // Source tile index s lies in chunk s / B; it pushes itself to the targets
 // s + 2 .. mid_end(s) - 1; the chunk product covers targets >= mid_end(s).
 __host__ __device__ __forceinline__ int mid_end(int s) { return (s / B + 2) * B; }
@@ -203,6 +228,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   __shared__ float2 sB[T][T + 2];   // E[I, J-1]; later W0 + X; later the tile's errors
   __shared__ float2 sGx[T][T + 1];  // full row-external sum of every entry
   const float sigma = P.hdr->sigma;
+  const float from_units = pow2f(fixed_unit_exp(sigma));
 
   // Loads in the natural mapping: rows a = warp + kRows t, column b = lane.
   const int b = lane;
@@ -226,8 +252,8 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     gf[t] = zero;
     if (va && vb) {
       const size_t o = (size_t)ra * P.n + cb;
-      c0[t] = df_add(df_add(make_float2(P.W[o], 0.f), P.Xm[o]), df_from_double(P.Xc[o]));
-      gf[t] = df_add(P.Gm[o], df_from_double(P.Gc[o]));
+      c0[t] = df_add(df_add(make_float2(P.W[o], 0.f), P.Xm[o]), df_from_fixed(P.Xc[o], from_units));
+      gf[t] = df_add(P.Gm[o], df_from_fixed(P.Gc[o], from_units));
     }
   }
   __syncthreads();
@@ -888,9 +914,14 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float d0 = rintf(u[2 * e]), d1 = rintf(u[2 * e + 1]);
-            const __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);  // low half: the smaller k
-            w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+            // Round to the nearest integer (ties to even) by adding and
+            // subtracting 1.5 * 2^23 (|u| <= 128.5: exact), on the fp32 pipes.
+            // The integer, of at most 8 significant bits, is exact in bf16:
+            // its bf16 pattern is the upper half of its fp32 pattern, and one
+            // byte permute packs two of them (low half: the smaller k).
+            const float d0 = (u[2 * e] + 0x1.8p23f) - 0x1.8p23f;
+            const float d1 = (u[2 * e + 1] + 0x1.8p23f) - 0x1.8p23f;
+            w[e] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
             u[2 * e] = (u[2 * e] - d0) * 256.f;  // exact: |u - d| <= 1/2, u has <= 24 significant bits
             u[2 * e + 1] = (u[2 * e + 1] - d1) * 256.f;
           }
@@ -931,16 +962,14 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
       mbar_wait(&sm.grp_full[h], (uint32_t)(gi >> 1) & 1u, broken);
       tc_fence_after();
       const int row0 = group_row0(gi), rows = group_rows(gi);
-      const int ex = sm.er[gi][r] + eD - 14;
+      // levels -> value: 2^(e_r + eD - 14); value -> fixed-point units: 2^-unit_exp
+      const int ex = sm.er[gi][r] + eD - 14 - fixed_unit_exp(P.hdr->sigma);
       const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
       // Output (row r, column q) of the group: column products update
-      // Xc[row0 + r][J*T + q], row products Gc[I*T + q][row0 + r].  The two
-      // chunk planes are fp64 and take each update as a reduction in L2
-      // (red.global.add.f64: no load, no wait).  A double-float value of at
-      // most 48 significant bits converts to fp64 exactly; an element gets at
-      // most one update per launch, so with one chunk stream its fp64
-      // additions (each rounded to 53 bits) come in a fixed order.
-      double* plane = cc.col ? P.Xc : P.Gc;
+      // Xc[row0 + r][J*T + q], row products Gc[I*T + q][row0 + r], each as
+      // one 64-bit integer reduction in L2 (red.global.add.u64: no load, no
+      // wait) of the fixed-point value (see fixed_unit_exp).
+      unsigned long long* plane = reinterpret_cast<unsigned long long*>(cc.col ? P.Xc : P.Gc);
       const int gr0 = cc.col ? row0 + r : cc.I * T, gc0 = cc.col ? cc.J * T : row0 + r;
       const bool rok = r < rows && (cc.col ? gr0 < P.m : gc0 < P.n);
       const size_t obase = rok ? (size_t)gr0 * P.n + gc0 : 0;
@@ -963,7 +992,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
           y = two_sum(y.x, y2.x);  // any level may be zero: no ordering of magnitudes holds
           y = two_sum(y.x, y.y + (y2.y + tail));
           if (rok && qb + j < qlim)
-            atomicAdd(plane + obase + (size_t)(qb + j) * ostep, ((double)y.x + (double)y.y) * (double)sc);
+            atomicAdd(plane + obase + (size_t)(qb + j) * ostep, (unsigned long long)df_to_fixed(y, sc));
         }
       }
       tc_fence_before();
@@ -1139,9 +1168,9 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.Wq = Wq;
   P.hdr = reinterpret_cast<Header*>(base);
   P.Xm = planes;
-  P.Xc = reinterpret_cast<double*>(planes + pstride);
+  P.Xc = reinterpret_cast<long long*>(planes + pstride);
   P.Gm = planes + 2 * pstride;
-  P.Gc = reinterpret_cast<double*>(planes + 3 * pstride);
+  P.Gc = reinterpret_cast<long long*>(planes + 3 * pstride);
   P.G = planes + 4 * pstride;
   P.E = planes + 5 * pstride;
   P.status = status_dev;
