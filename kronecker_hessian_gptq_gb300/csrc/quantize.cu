@@ -37,7 +37,8 @@
 // the entries of one anti-diagonal sit in one warp.  At in-tile step k that
 // warp rounds anti-diagonal k; after one barrier every
 // later entry folds in the one new term of its row sum (E[p, k-p] L_A[q, k-p])
-// and of its column sum (L_B[p, k-q] Gin[k-q, q], Gin = in-tile row sum + error).
+// and of its column sum (L_B[p, k-q] G[k-q, q], G = the full row transform,
+// published by each entry as it is rounded).
 //
 // Precision: every accumulation is double-float (df.cuh) or exact (the
 // digit products of the chunk products on the tensor cores, see that
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   __shared__ float sLA[T][T + 2];   // L_A[J, J]
   __shared__ float sLBo[T][T + 1];  // L_B[I, I-1]
   __shared__ float sLAo[T][T + 1];  // L_A[J, J-1]
-  __shared__ float2 sA[T][T + 2];   // G[I-1, J]; later the in-tile row transforms Gin
+  __shared__ float2 sA[T][T + 2];   // G[I-1, J]; later the tile's own G
   __shared__ float2 sB[T][T + 2];   // E[I, J-1]; later W0 + X; later the tile's errors
   __shared__ float2 sGx[T][T + 1];  // full row-external sum of every entry
   const float sigma = P.hdr->sigma;
@@ -276,10 +277,13 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   }
   __syncthreads();
 
-  // Skewed mapping.  acc: the tile input and the in-tile column terms;
-  // racc: the in-tile row terms (also needed alone, for the row transform
-  // Gin = racc + e).  Both offset accumulators share sigma, so the value to
-  // round is formed from them exactly when the entry's turn comes.
+  // Skewed mapping.  acc: the tile input, the distance-1 column pull and the
+  // in-tile column terms L_B[p, i] G[i, q] (i < p, in the tile); racc: the
+  // entry's row transform without its own error, i.e. its row-external sum
+  // plus the in-tile row terms, so that racc + e = G[p, q], the value the
+  // entry publishes for the column terms of the entries below it.  Both
+  // offset accumulators share sigma, so the value to round, acc + racc, is
+  // formed from them exactly when the entry's turn comes.
   const int p = lane;
   const int r = I * T + p;
   const bool vr = r < P.m;
@@ -291,17 +295,13 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     acc[j].init(sigma);
     racc[j].init(sigma);
     acc[j].mac(1.f, sB[p][qj[j]]);
+    racc[j].mac(1.f, sGx[p][qj[j]]);
   }
 #pragma unroll 4
   for (int i = 0; i < T; ++i) {  // distance-1 neighbour (I-1, J)
     const float l = sLBo[p][i];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) acc[j].mac(l, sA[i][qj[j]]);
-  }
-  for (int i = 0; i <= p; ++i) {  // L_B[I, I] times the row-external sums
-    const float l = sLB[p][i];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) acc[j].mac(l, sGx[i][qj[j]]);
   }
   const float s = (P.scales != nullptr && vr) ? P.scales[r] : 1.f;
   const float rcp = __frcp_rn(s);
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
         if (p + q > ks && ks >= 0) {
           if (jj >= 0 && jj < q) racc[j].mac(sLA[q][jj], et);                 // row term E[p, jj] L_A[q, jj]
           const int i = ks - q;
-          if (i >= 0 && i < p) acc[j].mac(sLB[p][i], sA[i][q]);                 // column term L_B[p, i] Gin[i, q]
+          if (i >= 0 && i < p) acc[j].mac(sLB[p][i], sA[i][q]);                 // column term L_B[p, i] G[i, q]
         }
         if (rounds_now && vr && J * T + q < P.n) {
           // (acc.H - sigma) and (racc.H - sigma) are exact and so is their
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
           const float2 h = two_sum(sv.x, -x.x);
           const float2 e = fast_two_sum(h.x, (sv.y - x.y) + h.y);
           sB[p][q] = e;
-          sA[p][q] = df_add(racc[j].value(sigma), e);  // Gin: the entry's in-tile row transform
+          sA[p][q] = df_add(racc[j].value(sigma), e);  // G[p, q]: the entry's full row transform
           vkeep[j] = v;
         }
       }
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     const int a = warp + kRows * t;
     const int ra = I * T + a;
     const float2 e = sB[a][b];
-    gv[t] = df_add(sGx[a][b], sA[a][b]);  // G = row-external sum + Gin
+    gv[t] = sA[a][b];  // G, published by the entry's rounding
     if (ra < P.m && vb) {
       const size_t o = (size_t)ra * P.n + cb;
       P.E[o] = e;
@@ -636,7 +636,8 @@ constexpr int kLevels = 6;       // levels 0 .. kDigD - 1
 constexpr int kTcM = 128;        // target rows per group (UC target tiles)
 constexpr int UC = kTcM / T;
 constexpr int kSlab = 32;        // k per slab of factor digits
-constexpr int kTcThreads = 12 * 32;
+constexpr int kTcWarps = 12;
+constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kGroupsPerCta = 8;  // target groups one chunk product CTA works through
 
 // Exponent of every (row, chunk) block of a d x d factor: out[r * nch + c]
@@ -740,8 +741,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, bool&
   return true;
 }
 
-// 8 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+// 4 or 8 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
@@ -756,8 +765,9 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Warp roles of a chunk product CTA.
 constexpr int kTcMmaWarp = 0;           // issues the tensor-core products (lane 0)
 constexpr int kTcEpiWarp0 = 4;          // warps 4..7: epilogue, tensor-memory lane quarters 0..3
-constexpr int kTcProducers = 7 * 32;    // warps 1..3 and 8..11: factor loads and digits
+constexpr int kTcProducers = (kTcWarps - 5) * 32;  // warps 1..3 and 8..: factor loads and digits
 constexpr int kTcStages = 3;            // fp32 factor slabs in flight per producer
+constexpr int kEpiCols = 8;             // output columns per epilogue step (registers: 6 levels each)
 
 struct TcSmem {
   __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
@@ -804,7 +814,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
   const bool is_epi = warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4;
   const bool is_prod = warp != kTcMmaWarp && !is_epi;
   const int ptid = is_prod ? (warp < kTcEpiWarp0 ? tid - 32 : tid - 160) : -1;  // 0 .. kTcProducers-1
-  static_assert(kTcThreads == 12 * 32 && kTcProducers == 7 * 32, "warp roles: 1 + 4 + 7");
+  static_assert(kTcWarps >= 9, "warp roles: 1 MMA + 4 epilogue + producers");
   const float* F = cc.col ? P.LB : P.LA;
   const signed char* fexp = cc.col ? P.expB : P.expA;
   const int d = cc.col ? P.m : P.n;
@@ -976,14 +986,14 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
       const size_t ostep = cc.col ? 1 : (size_t)P.n;  // next q
       const int qlim = cc.col ? P.n - gc0 : P.m - gr0;
 #pragma unroll 1
-      for (int qb = 0; qb < T; qb += 8) {
-        float lv[kLevels][8];
+      for (int qb = 0; qb < T; qb += kEpiCols) {
+        float lv[kLevels][kEpiCols];
 #pragma unroll
         for (int l = 0; l < kLevels; ++l)
-          tmem_ld8(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + 32 * l + qb), lv[l]);
+          tmem_ld(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + 32 * l + qb), lv[l]);
         asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kEpiCols; ++j) {
           // levels 0..2 exactly (each an integer sum below 2^24 on its own
           // grid), the rest (below 2^-24 of the total) in one fp32 sum
           float2 y = two_sum(lv[0][j], lv[1][j] * 0x1p-8f);
