@@ -280,8 +280,12 @@ def run_ours(args, rank, local_rank, world):
     out = (torch.empty((m, n), dtype=torch.int32, device=dev), torch.empty((m, n), dtype=torch.float32, device=dev),
            torch.zeros(1, dtype=torch.int32, device=dev))
     flush = torch.empty((512 << 20) // 4, dtype=torch.float32, device=dev)
+    if args.method == "gptq":  # row-wise GPTQ: the one-sided case B = I of the same solve
+        solve = lambda: bk.gptq(W, LA, s, p.bits, ws=ws, out=out)  # noqa: E731
+    else:
+        solve = lambda: bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)  # noqa: E731
     for _ in range(args.warmup):
-        bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)
+        solve()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
@@ -292,7 +296,7 @@ def run_ours(args, rank, local_rank, world):
     for k in range(args.steps):
         flush.zero_()
         starts[k].record()
-        bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)
+        solve()
         ends[k].record()
     torch.cuda.synchronize()
     barrier(world, dev)
@@ -301,6 +305,16 @@ def run_ours(args, rank, local_rank, world):
     if out[2].item() != 0:
         raise RuntimeError(f"device status {out[2].item()}")
     total_ms = aggregate_max(sum(step_ms), world, dev)
+    if args.method == "gptq":
+        cfg = workload_config(p, world)
+        cfg["method"] = "gptq (B = I)"
+        return {
+            "metric": "row-wise GPTQ solve time & weights quantized/s per m x n layer", "unit": UNIT,
+            "value": world * m * n * args.steps / (total_ms * 1e-3), "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32x2 double-float", "data": "synthetic", "config": cfg,
+            "prep_ms": prep_ms, "clocks": clocks, "roofline": None, "e2e": None, "gpu_launches": None,
+        }
 
     # Per-kernel timing pass (events around every launch), after the timed region.
     ncls = len(_lib.KERNEL_CLASSES)
@@ -376,6 +390,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq"],
+                    help="bakron (default, the headline) or gptq: row-wise GPTQ, the case B = I")
     args = ap.parse_args(argv)
     rank, local_rank, world = dist_env()
     if world > 1:

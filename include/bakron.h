@@ -137,6 +137,20 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
                     int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                     int32_t* status_dev, void* stream);
 
+/* -------------------------------------------------------- row-wise GPTQ
+ * The one-sided case B = I of the same solve: with L_B = I every row of W
+ * is quantized independently by Algorithm 1 with H = A, i.e. GPTQ ("BaKron:
+ * Efficient Quantization with Kronecker-Factored Hessians", Sec. 1: GPTQ's
+ * Hessian is X X^T (x) I; Sec. 3.1, Algorithm 1; the GPTQ column of
+ * Table 3).  Same arguments, conventions and results as bakron_quantize
+ * with LB the identity, without LB; the column terms, column pushes and
+ * column chunk products are skipped.  LA: the normalized factor of A (see
+ * bakron_factor).  Workspace: bakron_gptq_workspace_size(m, n) bytes.
+ */
+size_t bakron_gptq_workspace_size(int64_t m, int64_t n);
+int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, int bits, int64_t m, int64_t n,
+                         int32_t* V, float* Wq, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
 /* Diagnostics: bakron_quantize with CUDA events recorded around every
  * kernel launch, for per-kernel timing.  Same arguments and result as
  * bakron_quantize, plus three arrays of BAKRON_KERNEL_CLASSES entries

@@ -22,6 +22,7 @@ __all__ = [
     "prepare",
     "quantize",
     "quantize_host",
+    "gptq",
     "quantize_workspace_size",
     "prepare_workspace_size",
 ]
@@ -129,6 +130,30 @@ def quantize(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=No
     st = lib.bakron_quantize(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
                              _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
     _lib.check(st, "bakron_quantize")
+    return V, Wq, status
+
+
+def gptq(W, LA, scales=None, bits: int = 0, ws=None, out=None, stream=None):
+    """Row-wise GPTQ of W (m x n): the one-sided case B = I of quantize()
+    (bakron_gptq_quantize).  Returns (V, Wq, status) like quantize()."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    _require_cuda_f32(LA, (n, n), "LA")
+    if scales is not None:
+        _require_cuda_f32(scales, (m,), "scales")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, device=W.device)
+        Wq = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    else:
+        V, Wq, status = out
+    if ws is None:
+        ws = _workspace(lib.bakron_gptq_workspace_size(m, n), W.device)
+    st = lib.bakron_gptq_quantize(_ptr(W), _ptr(LA), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq), _ptr(ws),
+                                  ws.numel(), _ptr(status), _stream_handle(stream))
+    _lib.check(st, "bakron_gptq_quantize")
     return V, Wq, status
 
 

@@ -242,12 +242,12 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     const int ra = I * T + a;
     const bool va = ra < P.m;
     const int gc = I * T + b;
-    sLB[a][b] = (va && gc < P.m) ? (b < a ? P.LB[(size_t)ra * P.m + gc] : (b == a ? 1.f : 0.f)) : 0.f;
-    sLBo[a][b] = (I > 0 && va) ? P.LB[(size_t)ra * P.m + (I - 1) * T + b] : 0.f;
+    sLB[a][b] = (va && gc < P.m) ? (b < a ? (P.LB ? P.LB[(size_t)ra * P.m + gc] : 0.f) : (b == a ? 1.f : 0.f)) : 0.f;
+    sLBo[a][b] = (I > 0 && va && P.LB) ? P.LB[(size_t)ra * P.m + (I - 1) * T + b] : 0.f;
     const int rr = J * T + a, cc = J * T + b;
     sLA[a][b] = (rr < P.n && cc < P.n) ? (b < a ? P.LA[(size_t)rr * P.n + cc] : (b == a ? 1.f : 0.f)) : 0.f;
     sLAo[a][b] = (J > 0 && rr < P.n) ? P.LA[(size_t)rr * P.n + (J - 1) * T + b] : 0.f;
-    sA[a][b] = (I > 0 && vb) ? P.G[(size_t)((I - 1) * T + a) * P.n + cb] : zero;
+    sA[a][b] = (I > 0 && vb && P.LB) ? P.G[(size_t)((I - 1) * T + a) * P.n + cb] : zero;
     sB[a][b] = (J > 0 && va) ? P.E[(size_t)ra * P.n + (J - 1) * T + b] : zero;
     c0[t] = zero;
     gf[t] = zero;
@@ -297,11 +297,14 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     acc[j].mac(1.f, sB[p][qj[j]]);
     racc[j].mac(1.f, sGx[p][qj[j]]);
   }
+  const bool colterms = P.LB != nullptr;  // L_B = I (row-wise GPTQ): no column terms at all
+  if (colterms) {
 #pragma unroll 4
-  for (int i = 0; i < T; ++i) {  // distance-1 neighbour (I-1, J)
-    const float l = sLBo[p][i];
+    for (int i = 0; i < T; ++i) {  // distance-1 neighbour (I-1, J)
+      const float l = sLBo[p][i];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) acc[j].mac(l, sA[i][qj[j]]);
+      for (int j = 0; j < kPer; ++j) acc[j].mac(l, sA[i][qj[j]]);
+    }
   }
   const float s = (P.scales != nullptr && vr) ? P.scales[r] : 1.f;
   const float rcp = __frcp_rn(s);
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
         if (p + q > ks && ks >= 0) {
           if (jj >= 0 && jj < q) racc[j].mac(sLA[q][jj], et);                 // row term E[p, jj] L_A[q, jj]
           const int i = ks - q;
-          if (i >= 0 && i < p) acc[j].mac(sLB[p][i], sA[i][q]);                 // column term L_B[p, i] G[i, q]
+          if (colterms && i >= 0 && i < p) acc[j].mac(sLB[p][i], sA[i][q]);     // column term L_B[p, i] G[i, q]
         }
         if (rounds_now && vr && J * T + q < P.n) {
           // (acc.H - sigma) and (racc.H - sigma) are exact and so is their
@@ -389,10 +392,10 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   for (int t = 0; t < kPer; ++t) sGx[warp + kRows * t][b] = gv[t];
   __syncthreads();
 #pragma unroll
-  for (int t = 0; t < kPer; ++t) {  // G digits transposed: lane = row, coalesced along the row
+  for (int t = 0; t < kPer; ++t) {  // G digits transposed (column products only): lane = row, coalesced
     const int col = warp + kRows * t, row = lane;
     const int gr = I * T + row, gc = J * T + col;
-    if (gr < P.m && gc < P.n) put_digits(P.DGt, P.dstrideG, (size_t)gc * P.ldG + gr, sGx[row][col], dsc);
+    if (P.LB && gr < P.m && gc < P.n) put_digits(P.DGt, P.dstrideG, (size_t)gc * P.ldG + gr, sGx[row][col], dsc);
   }
 }
 
@@ -593,7 +596,7 @@ __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0)
   extern __shared__ __align__(16) unsigned char push_smem[];
   PushSmem<1>& sm = *reinterpret_cast<PushSmem<1>*>(push_smem);
   const int I = I0 + blockIdx.x, J = K - I;
-  const int c_first = I + 2, c_end = min(P.Mt, mid_end(I));
+  const int c_first = I + 2, c_end = P.LB ? min(P.Mt, mid_end(I)) : c_first;  // L_B = I: no column pushes
   const int r_first = J + 2, r_end = min(P.Nt, mid_end(J));
   const int ncu = c_end > c_first ? (c_end - c_first + U - 1) / U : 0;
   const int nru = r_end > r_first ? (r_end - r_first + U - 1) / U : 0;
@@ -1233,7 +1236,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
     signed char* eB = reinterpret_cast<signed char*>(base + lay.expB);
     const size_t wA = (size_t)n * P.nchA, wB = (size_t)m * P.nchB;  // one warp per (row, chunk)
     factor_exp_kernel<<<(unsigned)((wA + 7) / 8), 256, 0, stream>>>(LA, n, P.nchA, eA);
-    factor_exp_kernel<<<(unsigned)((wB + 7) / 8), 256, 0, stream>>>(LB, m, P.nchB, eB);
+    if (LB) factor_exp_kernel<<<(unsigned)((wB + 7) / 8), 256, 0, stream>>>(LB, m, P.nchB, eB);
   }
   clock.end(0.0);
   cudaEventRecord(ev_start, stream);
@@ -1264,7 +1267,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
     double mid_tiles = 0;
     for (int I = I0; I <= I1; ++I) {
       const int J = K - I;
-      mid_tiles += std::max(0, std::min(P.Mt, mid_end(I)) - (I + 2));
+      if (LB) mid_tiles += std::max(0, std::min(P.Mt, mid_end(I)) - (I + 2));
       mid_tiles += std::max(0, std::min(P.Nt, mid_end(J)) - (J + 2));
     }
     if (mid_tiles > 0) {
@@ -1279,7 +1282,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
     }
 
     // chunk products closed by K
-    const int ncc = std::min(K, P.Mt - 1) >= B - 1 ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
+    const int ncc = (LB && std::min(K, P.Mt - 1) >= B - 1) ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
     const int ncr = std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0;
     double chunk_tiles = 0;
     int chunk_most = 0;  // most targets of one candidate

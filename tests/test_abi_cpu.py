@@ -102,3 +102,18 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "missing.so"))
     finally:
         _lib._lib = saved
+
+
+def test_gptq_entry_point_rejects_bad_arguments(lib):
+    W = ctypes.c_void_p(0x1000)
+    V, Wq = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    ws = ctypes.c_void_p(0x100000)
+    big = lib.bakron_gptq_workspace_size(8, 8)
+    assert big == lib.bakron_quantize_workspace_size(8, 8)
+    g = lib.bakron_gptq_quantize
+    assert g(W, W, None, 4, 0, 8, V, Wq, ws, big, W, None) == 1  # m < 1
+    assert g(None, W, None, 4, 8, 8, V, Wq, ws, big, W, None) == 1  # null W
+    assert g(W, None, None, 4, 8, 8, V, Wq, ws, big, W, None) == 1  # null LA
+    assert g(W, W, None, 9, 8, 8, V, Wq, ws, big, W, None) == 1  # bits
+    assert g(W, W, None, 4, 8, 8, V, W, ws, big, W, None) == 1  # Wq aliases W
+    assert g(W, W, None, 4, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
