@@ -37,6 +37,15 @@ What is here, and what pins it (the pins live in ``tests/test_oracle_*.py``):
   metrics.*                         distortion tr(A (Wq-W)^T B (Wq-W)) and the
       two exact identities Wq - W = L_B E L_A^T and
       distortion = sum_ij E_ij^2 R_B,ii^2 R_A,jj^2, and Corollary 3.4's bound.
+  quantizer.alphabet_bounds         also explicit alphabets (lo, hi), e.g. the
+      symmetric {-l .. l} of App. D.  Pinned by clamped round-to-nearest
+      when A and B are diagonal.
+  scales.row_scales                 App. D scale choice (absmax / l, MSE
+      shrink search up to 2x).  Pinned by hand-worked rows (tests/golden/
+      row_scales.json), rows of equal magnitudes (zero error at the full
+      scale) and the no-search case.
+  scales.pack_codes / unpack_codes  b-bit two's complement packing.  Pinned
+      by hand-packed bytes (tests/golden/pack_codes.json) and round trips.
 
 No function here is "parity unpinned".
 
@@ -49,6 +58,7 @@ then formed in float64 from the float64 value x.
 
 from .factors import normalized_inv_cholesky, rev_cholesky  # noqa: F401
 from .quantizer import alphabet_bounds, quantize  # noqa: F401
+from .scales import pack_codes, row_error, row_scales, shrink_factors, unpack_codes  # noqa: F401
 from .naive import bakron_naive, babai_nearest_plane, gptq_rows  # noqa: F401
 from .antidiag import bakron_antidiagonal, bakron_definition  # noqa: F401
 from .recursive import bakron_alg6, bakron_recursive  # noqa: F401

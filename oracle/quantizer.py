@@ -23,8 +23,16 @@ from typing import Optional, Tuple
 import numpy as np
 
 
-def alphabet_bounds(bits: int) -> Optional[Tuple[int, int]]:
-    """(lo, hi) of the alphabet for ``bits`` > 0, or None for Z."""
+def alphabet_bounds(bits) -> Optional[Tuple[int, int]]:
+    """(lo, hi) of the alphabet for ``bits`` > 0, or None for Z.
+
+    ``bits`` may also be an explicit integer alphabet (lo, hi), lo < hi: the
+    symmetric {-l .. l} of App. D is (-l, l)."""
+    if isinstance(bits, tuple):
+        lo, hi = int(bits[0]), int(bits[1])
+        if not lo < hi:
+            raise ValueError("an explicit alphabet needs lo < hi")
+        return lo, hi
     if bits == 0:
         return None
     if bits < 2:
@@ -33,7 +41,7 @@ def alphabet_bounds(bits: int) -> Optional[Tuple[int, int]]:
     return -half, half - 1
 
 
-def quantize(x, s, bits: int):
+def quantize(x, s, bits):
     """Integer codes v and float64 errors e = s*v - x for values x (float64).
 
     ``s`` is a float32 scale broadcastable to x, or None for scale 1.
