@@ -151,6 +151,55 @@ size_t bakron_gptq_workspace_size(int64_t m, int64_t n);
 int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, int bits, int64_t m, int64_t n,
                          int32_t* V, float* Wq, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
 
+/* -------------------------------------------- alphabets, scales, packing
+ * The base quantizer's variants ("BaKron: Efficient Quantization with
+ * Kronecker-Factored Hessians", App. D: per-output-feature scales from the
+ * row's largest magnitude over the alphabet's reach, optionally shrunk by up
+ * to a factor 2 by a mean-squared-error search; Sec. 3.1: integer
+ * alphabets).
+ */
+#define BAKRON_MAX_CODE 32767
+#define BAKRON_MAX_SCALE_GRID 256
+
+/* bakron_quantize over an explicit integer alphabet {lo .. hi}:
+ *     v_ij = clamp(round_half_even(fp32(W~_ij) / s_i), lo, hi).
+ * lo <= 0 <= hi, lo < hi, |lo|, |hi| <= BAKRON_MAX_CODE; the symmetric
+ * alphabet {-l .. l} of App. D is lo = -l, hi = l, and bits = b of
+ * bakron_quantize is lo = -2^(b-1), hi = 2^(b-1) - 1.  LB may be NULL: then
+ * L_B = I and the call is the row-wise GPTQ solve of bakron_gptq_quantize.
+ * Every other argument, result and error as in bakron_quantize.
+ */
+int bakron_quantize_range(const float* W, const float* LA, const float* LB, const float* scales, int lo, int hi,
+                          int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                          int32_t* status_dev, void* stream);
+
+/* Per-row scales for the alphabet {lo .. hi} (lo < 0 < hi), App. D:
+ *     s0_i = fp32(max_j |W_ij| / hi)      (correctly rounded fp32 division),
+ *     f_g = fp32(1 - g / (2 (grid - 1))),  g = 0 .. grid-1 (1 down to 1/2),
+ *     err_i(s) = sum_j (W_ij - s v_ij)^2,  v_ij = clamp(round_half_even(
+ *                fp32(W_ij) / s), lo, hi),
+ *     scales[i] = fp32(s0_i f_g) for the g of least err_i, the smallest g
+ *                among equal errors.
+ * grid = 1: scales[i] = s0_i (no search); 1 <= grid <= BAKRON_MAX_SCALE_GRID.
+ * A row without a nonzero entry gets scale 1.  The errors are summed in
+ * double-float (each term exact), so two candidates whose errors differ
+ * by less than about 1e-12 relative may be ordered either way.
+ * W: device, m x n, finite (a row holding a NaN or infinity gets an
+ *    unspecified scale); scales: device, m floats, distinct from W.
+ * m, n >= 1, m * n < 2^31.  One CTA per row; enqueued on `stream`.
+ */
+int bakron_row_scales(const float* W, int64_t m, int64_t n, int lo, int hi, int grid, float* scales, void* stream);
+
+/* Packed codes: each code of V (device int32, m x n) as its `bits`-bit two's
+ * complement, bits in {2, 4, 8}; code j of row i sits in byte
+ * i * ceil(n bits / 8) + floor(j bits / 8) of `out` at bit offset
+ * (j bits) mod 8 (little-endian within a byte); each row starts at a byte
+ * boundary and a row's unused high bits are zero.  Codes outside
+ * {-2^(bits-1) .. 2^(bits-1) - 1} keep only their low `bits` bits.
+ * out: device, m * ceil(n bits / 8) bytes.  Enqueued on `stream`.
+ */
+int bakron_pack_codes(const int32_t* V, int64_t m, int64_t n, int bits, uint8_t* out, void* stream);
+
 /* Diagnostics: bakron_quantize with CUDA events recorded around every
  * kernel launch, for per-kernel timing.  Same arguments and result as
  * bakron_quantize, plus three arrays of BAKRON_KERNEL_CLASSES entries

@@ -23,6 +23,9 @@ __all__ = [
     "quantize",
     "quantize_host",
     "gptq",
+    "quantize_range",
+    "row_scales",
+    "pack_codes",
     "quantize_workspace_size",
     "prepare_workspace_size",
 ]
@@ -155,6 +158,66 @@ def gptq(W, LA, scales=None, bits: int = 0, ws=None, out=None, stream=None):
                                   ws.numel(), _ptr(status), _stream_handle(stream))
     _lib.check(st, "bakron_gptq_quantize")
     return V, Wq, status
+
+
+def quantize_range(W, LA, LB, scales, lo: int, hi: int, ws=None, out=None, stream=None):
+    """BaKron (LB given) or row-wise GPTQ (LB None) over the integer alphabet
+    {lo .. hi} (bakron_quantize_range).  Returns (V, Wq, status) like
+    quantize()."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    _require_cuda_f32(LA, (n, n), "LA")
+    if LB is not None:
+        _require_cuda_f32(LB, (m, m), "LB")
+    if scales is not None:
+        _require_cuda_f32(scales, (m,), "scales")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, device=W.device)
+        Wq = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    else:
+        V, Wq, status = out
+    if ws is None:
+        ws = _workspace(lib.bakron_quantize_workspace_size(m, n), W.device)
+    st = lib.bakron_quantize_range(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(lo), int(hi), m, n, _ptr(V),
+                                   _ptr(Wq), _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
+    _lib.check(st, "bakron_quantize_range")
+    return V, Wq, status
+
+
+def row_scales(W, lo: int, hi: int, grid: int = 1, out=None, stream=None):
+    """Per-row scales of W for the alphabet {lo .. hi}, with a shrink search
+    over `grid` factors from 1 down to 1/2 (bakron_row_scales).  Returns a
+    float32 CUDA tensor of m scales."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    scales = torch.empty(m, dtype=torch.float32, device=W.device) if out is None else out
+    _require_cuda_f32(scales, (m,), "scales")
+    st = lib.bakron_row_scales(_ptr(W), m, n, int(lo), int(hi), int(grid), _ptr(scales), _stream_handle(stream))
+    _lib.check(st, "bakron_row_scales")
+    return scales
+
+
+def pack_codes(V, bits: int, out=None, stream=None):
+    """The codes V (int32, m x n) packed as bits-bit two's complement, rows
+    byte-aligned (bakron_pack_codes).  Returns a uint8 CUDA tensor of
+    m x ceil(n bits / 8)."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = V.shape
+    if not (V.is_cuda and V.dtype == torch.int32 and V.is_contiguous()):
+        raise ValueError("V must be a contiguous int32 CUDA tensor")
+    rowbytes = (n * int(bits) + 7) // 8
+    P = torch.empty((m, rowbytes), dtype=torch.uint8, device=V.device) if out is None else out
+    if not (P.is_cuda and P.dtype == torch.uint8 and P.is_contiguous() and tuple(P.shape) == (m, rowbytes)):
+        raise ValueError("out must be a contiguous uint8 CUDA tensor of m x ceil(n bits / 8)")
+    st = lib.bakron_pack_codes(_ptr(V), m, n, int(bits), _ptr(P), _stream_handle(stream))
+    _lib.check(st, "bakron_pack_codes")
+    return P
 
 
 def quantize_host(W, LA, LB, scales=None, bits: int = 0, dev_ws=None, out=None, stream=None) -> Tuple:

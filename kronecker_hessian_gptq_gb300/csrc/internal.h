@@ -20,11 +20,26 @@ struct KernelTimer {
   double flops[kKernelClasses];  // algorithmic flops (2 per multiply-add) of the class
 };
 
-// quantize.cu
+// Integer alphabet of the rounding: {lo .. hi} when bounded, else Z.
+struct Alphabet {
+  bool bounded;
+  int lo, hi;
+};
+// `bits` = 0: Z; 2..8: {-2^(bits-1) .. 2^(bits-1) - 1}.
+inline Alphabet alphabet_from_bits(int bits) {
+  return bits ? Alphabet{true, -(1 << (bits - 1)), (1 << (bits - 1)) - 1} : Alphabet{false, 0, 0};
+}
+
+// quantize.cu (LB == nullptr: the output factor is the identity, row-wise GPTQ)
 size_t quantize_workspace_bytes(int64_t m, int64_t n);
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
-                            int bits, int m, int n, int32_t* V, float* Wq, void* ws,
+                            Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
+
+// scales.cu
+cudaError_t row_scales_launch(const float* W, int m, int n, Alphabet al, int grid, float* scales,
+                              cudaStream_t stream);
+cudaError_t pack_codes_launch(const int32_t* V, int m, int n, int bits, uint8_t* out, cudaStream_t stream);
 
 // prep.cu
 size_t factor_workspace_bytes(int64_t d);

@@ -138,7 +138,7 @@ __global__ void prepass_kernel(QParams P) {
 __global__ void sigma_kernel(QParams P) {
   const float maxw = __uint_as_float(P.hdr->maxw_bits);
   const float maxs = P.scales ? __uint_as_float(P.hdr->maxs_bits) : 1.f;
-  const float levels = P.bits ? (float)(1 << (P.bits - 1)) : 1.f;
+  const float levels = P.bits ? (float)max(-P.lo, P.hi) : 1.f;
   // Every value rounded or accumulated stays within a few alphabet steps of
   // the weights; the offset leaves a wide margin above that.
   P.hdr->sigma = offset_for_bound(16.f * (maxw + maxs * (levels + 2.f)));
@@ -345,9 +345,10 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
           // sum (two multiples of the offset's half-ulp, below sigma).
           const float2 x = two_sum((acc[j].H - sigma) + (racc[j].H - sigma), acc[j].L + racc[j].L);
           // fp32 decision: x.x == fp32(x); x.x * rcp is within 2 ulp of the
-          // correctly rounded quotient, which is used near a rounding tie.
+          // correctly rounded quotient, which is used near a rounding tie
+          // (and for an infinite or NaN product: a scale below 2^-128).
           float y = x.x * rcp;
-          if (fabsf(y) > 256.f || fabsf(y - floorf(y) - 0.5f) < 1e-3f) y = __fdiv_rn(x.x, s);
+          if (!(fabsf(y) <= 256.f) || fabsf(y - floorf(y) - 0.5f) < 1e-3f) y = __fdiv_rn(x.x, s);
           float v = rintf(y);
           if (P.bits) v = fminf(fmaxf(v, flo), fhi);
           // e = s v - x: exact high-word difference, then the low words
@@ -1158,7 +1159,7 @@ WsLayout ws_layout(int64_t m, int64_t n) {
 size_t quantize_workspace_bytes(int64_t m, int64_t n) { return ws_layout(m, n).total; }
 
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
-                            int bits, int m, int n, int32_t* V, float* Wq, void* ws,
+                            Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
   const WsLayout lay = ws_layout(m, n);
   const size_t plane = lay.plane;
@@ -1194,9 +1195,9 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.n = n;
   P.Mt = (m + T - 1) / T;
   P.Nt = (n + T - 1) / T;
-  P.bits = bits;
-  P.lo = bits ? -(1 << (bits - 1)) : 0;
-  P.hi = bits ? (1 << (bits - 1)) - 1 : 0;
+  P.bits = al.bounded ? 1 : 0;  // 1: the codes are clamped to {lo .. hi}
+  P.lo = al.lo;
+  P.hi = al.hi;
   const int Kmax = P.Mt + P.Nt - 2;
 
   int dev = 0;

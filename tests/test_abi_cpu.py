@@ -117,3 +117,32 @@ def test_gptq_entry_point_rejects_bad_arguments(lib):
     assert g(W, W, None, 9, 8, 8, V, Wq, ws, big, W, None) == 1  # bits
     assert g(W, W, None, 4, 8, 8, V, W, ws, big, W, None) == 1  # Wq aliases W
     assert g(W, W, None, 4, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
+
+
+def test_range_scales_and_pack_entry_points_reject_bad_arguments(lib):
+    W = ctypes.c_void_p(0x1000)
+    V, Wq, S = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000)
+    ws = ctypes.c_void_p(0x100000)
+    big = lib.bakron_quantize_workspace_size(8, 8)
+    q = lib.bakron_quantize_range
+    assert q(W, W, None, None, -8, 7, 0, 8, V, Wq, ws, big, W, None) == 1  # m < 1
+    assert q(W, None, None, None, -8, 7, 8, 8, V, Wq, ws, big, W, None) == 1  # null LA
+    assert q(W, W, None, None, 7, -8, 8, 8, V, Wq, ws, big, W, None) == 1  # lo > hi
+    assert q(W, W, None, None, 3, 3, 8, 8, V, Wq, ws, big, W, None) == 1  # lo == hi
+    assert q(W, W, None, None, 1, 7, 8, 8, V, Wq, ws, big, W, None) == 1  # 0 not a code
+    assert q(W, W, None, None, -40000, 7, 8, 8, V, Wq, ws, big, W, None) == 1  # |lo| too large
+    assert q(W, W, None, None, -8, 7, 8, 8, V, V, ws, big, W, None) == 1  # V aliases Wq
+    assert q(W, W, None, None, -8, 7, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
+    r = lib.bakron_row_scales
+    assert r(W, 0, 8, -8, 7, 1, S, None) == 1  # m < 1
+    assert r(W, 8, 8, 0, 7, 1, S, None) == 1  # lo must be negative
+    assert r(W, 8, 8, -8, 0, 1, S, None) == 1  # hi must be positive
+    assert r(W, 8, 8, -8, 7, 0, S, None) == 1  # grid < 1
+    assert r(W, 8, 8, -8, 7, 257, S, None) == 1  # grid above the table
+    assert r(W, 8, 8, -8, 7, 4, W, None) == 1  # scales alias W
+    assert r(None, 8, 8, -8, 7, 4, S, None) == 1  # null W
+    p = lib.bakron_pack_codes
+    assert p(V, 8, 8, 3, S, None) == 1  # bits not in {2, 4, 8}
+    assert p(V, 8, 0, 4, S, None) == 1  # n < 1
+    assert p(None, 8, 8, 4, S, None) == 1  # null V
+    assert p(V, 8, 8, 4, None, None) == 1  # null out
