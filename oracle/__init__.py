@@ -46,6 +46,12 @@ What is here, and what pins it (the pins live in ``tests/test_oracle_*.py``):
       scale) and the no-search case.
   scales.pack_codes / unpack_codes  b-bit two's complement packing.  Pinned
       by hand-packed bytes (tests/golden/pack_codes.json) and round trips.
+  scales.element_scales             one scale per entry from per-row or
+      per-run (group) scales and optional column scales (Sec. 3.1).  Pinned
+      by hand-worked matrices; every solver accepts an m x n scale matrix,
+      pinned by the naive solve on vec(W), per-entry rounding for diagonal
+      factors, and power-of-two column scales as a change of variables
+      (W D^-1, D A D) with identical codes.
 
 No function here is "parity unpinned".
 
@@ -58,7 +64,7 @@ then formed in float64 from the float64 value x.
 
 from .factors import normalized_inv_cholesky, rev_cholesky  # noqa: F401
 from .quantizer import alphabet_bounds, quantize  # noqa: F401
-from .scales import pack_codes, row_error, row_scales, shrink_factors, unpack_codes  # noqa: F401
+from .scales import element_scales, pack_codes, row_error, row_scales, shrink_factors, unpack_codes  # noqa: F401
 from .naive import bakron_naive, babai_nearest_plane, gptq_rows  # noqa: F401
 from .antidiag import bakron_antidiagonal, bakron_definition  # noqa: F401
 from .recursive import bakron_alg6, bakron_recursive  # noqa: F401

@@ -16,7 +16,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .quantizer import quantize
+from .quantizer import quantize, scale_at
 
 
 def antidiagonal_indices(m: int, n: int, k: int):
@@ -27,8 +27,6 @@ def antidiagonal_indices(m: int, n: int, k: int):
     return rows, k - rows
 
 
-def _row_scales(scales, rows):
-    return None if scales is None else np.asarray(scales, dtype=np.float32)[rows]
 
 
 def bakron_definition(W, LA, LB, scales, bits: int):
@@ -45,7 +43,7 @@ def bakron_definition(W, LA, LB, scales, bits: int):
     for k in range(m + n - 1):
         rows, cols = antidiagonal_indices(m, n, k)
         Wt = W0 + LB @ E @ LA.T  # E is zero on anti-diagonals >= k
-        v, e = quantize(Wt[rows, cols], _row_scales(scales, rows), bits)
+        v, e = quantize(Wt[rows, cols], scale_at(scales, rows, cols), bits)
         V[rows, cols] = v
         E[rows, cols] = e
     Wq = W0 + LB @ E @ LA.T
@@ -66,7 +64,7 @@ def bakron_antidiagonal(W, LA, LB, scales, bits: int):
     E = np.zeros((m, n))
     for k in range(m + n - 1):
         rows, cols = antidiagonal_indices(m, n, k)
-        v, delta = quantize(Wk[rows, cols], _row_scales(scales, rows), bits)
+        v, delta = quantize(Wk[rows, cols], scale_at(scales, rows, cols), bits)
         V[rows, cols] = v
         E[rows, cols] = delta
         # L_B Delta L_A^T with Delta supported on the anti-diagonal

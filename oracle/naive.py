@@ -25,10 +25,12 @@ from .quantizer import quantize
 
 
 def _vec_scales(scales: Optional[np.ndarray], m: int, n: int) -> Optional[np.ndarray]:
-    """Scale of every coordinate of vec(W): coordinate t lies in row t mod m."""
+    """Scale of every coordinate of vec(W): coordinate t is entry (t mod m,
+    t div m).  ``scales``: one per row (m,) or one per entry (m, n)."""
     if scales is None:
         return None
-    return np.tile(np.asarray(scales, dtype=np.float32), n)
+    s = np.asarray(scales, dtype=np.float32)
+    return np.tile(s, n) if s.ndim == 1 else s.flatten(order="F")
 
 
 def gptq_vector(w: np.ndarray, Lhat: np.ndarray, s: Optional[np.ndarray], bits: int):
@@ -108,6 +110,10 @@ def gptq_rows(W, A, scales, bits: int):
     E = np.zeros((m, n))
     Wq = np.zeros((m, n))
     for i in range(m):
-        s = None if scales is None else np.full(n, np.float32(scales[i]), dtype=np.float32)
+        if scales is None:
+            s = None
+        else:
+            sc = np.asarray(scales, dtype=np.float32)
+            s = np.full(n, sc[i], dtype=np.float32) if sc.ndim == 1 else sc[i]
         V[i], E[i], Wq[i] = gptq_vector(W[i], Lhat, s, bits)
     return V, Wq, E

@@ -63,3 +63,23 @@ def quantize(x, s, bits):
     v = v.astype(np.int64)
     e = s64 * v.astype(np.float64) - x
     return v, e
+
+
+def scale_at(scales, rows, cols):
+    """The float32 scales of entries (rows[k], cols[k]): ``scales`` is None
+    (scale 1), one scale per row (shape (m,)), or one per entry (shape
+    (m, n); see oracle.scales.element_scales for row, group and column
+    scales)."""
+    if scales is None:
+        return None
+    s = np.asarray(scales, dtype=np.float32)
+    return s[rows] if s.ndim == 1 else s[rows, cols]
+
+
+def scale_grid(scales, m: int, n: int):
+    """The m x n float64 matrix of every entry's scale (1 for None)."""
+    if scales is None:
+        return np.ones((m, n))
+    s = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    return np.broadcast_to(s[:, None] if s.ndim == 1 else s, (m, n))
+

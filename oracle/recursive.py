@@ -26,7 +26,7 @@ import sys
 import numpy as np
 
 from .antidiag import antidiagonal_indices
-from .quantizer import quantize
+from .quantizer import quantize, scale_at, scale_grid
 
 
 def _scales32(scales):
@@ -56,7 +56,7 @@ def bakron_recursive(W, LA, LB, scales, bits: int, leaf: int = 64):
         mm, nn = r1 - r0, c1 - c0
         for k in range(mm + nn - 1):
             rows, cols = antidiagonal_indices(mm, nn, k)
-            v, d = quantize(blk[rows, cols], None if s is None else s[r0 + rows], bits)
+            v, d = quantize(blk[rows, cols], scale_at(s, r0 + rows, c0 + cols), bits)
             V[r0 + rows, c0 + cols] = v
             E[r0 + rows, c0 + cols] = d
             blk += (lb[:, rows] * d[None, :]) @ la[:, cols].T
@@ -64,7 +64,7 @@ def bakron_recursive(W, LA, LB, scales, bits: int, leaf: int = 64):
     def solve(r0, r1, c0, c1):
         mm, nn = r1 - r0, c1 - c0
         if mm == 1 and nn == 1:
-            v, d = quantize(Wk[r0, c0], None if s is None else s[r0], bits)
+            v, d = quantize(Wk[r0, c0], scale_at(s, r0, c0), bits)
             V[r0, c0] = v
             E[r0, c0] = d
         elif leaf > 1 and mm <= leaf and nn <= leaf:
@@ -86,7 +86,7 @@ def bakron_recursive(W, LA, LB, scales, bits: int, leaf: int = 64):
         solve(0, m, 0, n)
     finally:
         sys.setrecursionlimit(old)
-    Wq = (1.0 if s is None else s.astype(np.float64)[:, None]) * V
+    Wq = scale_grid(s, m, n) * V
     return V, Wq, E
 
 
@@ -107,7 +107,7 @@ def bakron_alg6(W, LA, LB, scales, bits: int):
     def solve(k, l):
         if l == k + 1:
             rows, cols = antidiagonal_indices(m, n, k)
-            v, d = quantize(Wk[rows, cols], None if s is None else s[rows], bits)
+            v, d = quantize(Wk[rows, cols], scale_at(s, rows, cols), bits)
             V[rows, cols] = v
             E[rows, cols] = d
             return
@@ -119,5 +119,5 @@ def bakron_alg6(W, LA, LB, scales, bits: int):
         solve(mid, l)
 
     solve(0, m + n - 1)
-    Wq = (1.0 if s is None else s.astype(np.float64)[:, None]) * V
+    Wq = scale_grid(s, m, n) * V
     return V, Wq, E

@@ -17,6 +17,15 @@ spell the search out; the reading used here is the plain one:
 
 G = 1 means no search (s0).  A row of zeros gets scale 1.
 
+Groups and column scales (Sec. 3.1: scales "for each row and/or column";
+App. D itself uses per-row scales, no groups).  The reading used: with a
+group size g, row i holds one scale per run of g consecutive columns, each
+chosen by the search above on that run alone (g >= n: one per row); column
+scales t_j, where given, multiply in, and an entry's scale is the product
+rounded once to fp32,
+    sigma_ij = fp32(R[i, floor(j / g)] * t_j)  (sigma_ij = R[i, floor(j / g)]
+without column scales); the alphabet of entry (i, j) is sigma_ij {lo .. hi}.
+
 Packed codes: each code v in {lo .. hi}, lo >= -2^(b-1), hi < 2^(b-1), is
 stored as its b-bit two's complement, b in {2, 4, 8}; code j of a row sits
 in byte floor(j b / 8) at bit offset (j b) mod 8 (little-endian within the
@@ -48,11 +57,23 @@ def row_error(w, s, lo: int, hi: int) -> float:
     return float(np.dot(e, e))
 
 
-def row_scales(W, lo: int, hi: int, grid: int = 1):
-    """Per-row scales (float32) and, per row, the index g chosen."""
+def row_scales(W, lo: int, hi: int, grid: int = 1, group=None):
+    """Per-row scales (float32) and, per row, the index g chosen; with a
+    ``group`` size, an (m, ceil(n / group)) array of per-run scales (and
+    indices) instead."""
     if not (lo < 0 < hi):
         raise ValueError("the alphabet must contain negative and positive codes")
     W = np.asarray(W, dtype=np.float32)
+    if group is not None:
+        if group < 1:
+            raise ValueError("group >= 1")
+        m, n = W.shape
+        ng = max(1, -(-n // group))
+        S = np.empty((m, ng), dtype=np.float32)
+        C = np.zeros((m, ng), dtype=np.int64)
+        for k in range(ng):
+            S[:, k], C[:, k] = row_scales(W[:, k * group:(k + 1) * group], lo, hi, grid)
+        return S, C
     f = shrink_factors(grid)
     scales = np.empty(W.shape[0], dtype=np.float32)
     chosen = np.zeros(W.shape[0], dtype=np.int64)
@@ -71,6 +92,25 @@ def row_scales(W, lo: int, hi: int, grid: int = 1):
         scales[i] = np.float32(s0 * f[best])
         chosen[i] = best
     return scales, chosen
+
+
+def element_scales(R, n: int, group=None, col_scales=None) -> np.ndarray:
+    """The m x n float32 scale of every entry: fp32(R[i, floor(j / g)] t_j).
+
+    R: per-row scales (m,) (no groups) or per-run scales (m, ceil(n / g)).
+    col_scales: n column scales t_j, or None (all ones, no rounding)."""
+    R = np.asarray(R, dtype=np.float32)
+    if R.ndim == 1:
+        R = R[:, None]
+    g = n if group is None else int(group)
+    cols = np.arange(n) // g
+    if R.shape[1] != max(1, -(-n // g)):
+        raise ValueError("R must hold ceil(n / group) scales per row")
+    S = R[:, cols]
+    if col_scales is None:
+        return np.ascontiguousarray(S)
+    t = np.asarray(col_scales, dtype=np.float32)
+    return (S.astype(np.float64) * t.astype(np.float64)[None, :]).astype(np.float32)
 
 
 def pack_codes(V, bits: int) -> np.ndarray:
