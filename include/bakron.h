@@ -173,6 +173,23 @@ int bakron_quantize_range(const float* W, const float* LA, const float* LB, cons
                           int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                           int32_t* status_dev, void* stream);
 
+/* bakron_quantize_range with one scale per entry (Sec. 3.1: scales "for
+ * each row and/or column"):
+ *     sigma_ij = fp32(scales[i][j / group] * col_scales[j]),
+ *     v_ij = clamp(round_half_even(fp32(W~_ij) / sigma_ij), lo, hi),
+ *     Wq_ij = fp32(sigma_ij v_ij).
+ * scales: device, m x ceil(n / group) row-major (one scale per run of
+ *     `group` consecutive columns of a row), or NULL for ones.
+ * group: columns per run; 0 (or >= n) for one scale per row (m scales).
+ * col_scales: device, n column scales, or NULL (then sigma_ij is the run's
+ *     scale itself, no rounding).
+ * All scales > 0 and finite (else BAKRON_DEV_BAD_SCALE in *status_dev).
+ * LB may be NULL (L_B = I).  Everything else as bakron_quantize_range.
+ */
+int bakron_quantize_scaled(const float* W, const float* LA, const float* LB, const float* scales, int64_t group,
+                           const float* col_scales, int lo, int hi, int64_t m, int64_t n, int32_t* V, float* Wq,
+                           void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
 /* Per-row scales for the alphabet {lo .. hi} (lo < 0 < hi), App. D:
  *     s0_i = fp32(max_j |W_ij| / hi)      (correctly rounded fp32 division),
  *     f_g = fp32(1 - g / (2 (grid - 1))),  g = 0 .. grid-1 (1 down to 1/2),
@@ -184,11 +201,16 @@ int bakron_quantize_range(const float* W, const float* LA, const float* LB, cons
  * A row without a nonzero entry gets scale 1.  The errors are summed in
  * double-float (each term exact), so two candidates whose errors differ
  * by less than about 1e-12 relative may be ordered either way.
- * W: device, m x n, finite (a row holding a NaN or infinity gets an
- *    unspecified scale); scales: device, m floats, distinct from W.
- * m, n >= 1, m * n < 2^31.  One CTA per row; enqueued on `stream`.
+ * group: 0 (or >= n) for one scale per row; else one scale per run of
+ *    `group` consecutive columns of each row, each run searched on its own
+ *    entries (the last run may be shorter), scales[i][k] row-major,
+ *    m x ceil(n / group) -- the layout bakron_quantize_scaled reads.
+ * W: device, m x n, finite (a run holding a NaN or infinity gets an
+ *    unspecified scale); scales: device, distinct from W.
+ * m, n >= 1, m * n < 2^31.  One CTA per run; enqueued on `stream`.
  */
-int bakron_row_scales(const float* W, int64_t m, int64_t n, int lo, int hi, int grid, float* scales, void* stream);
+int bakron_row_scales(const float* W, int64_t m, int64_t n, int64_t group, int lo, int hi, int grid, float* scales,
+                      void* stream);
 
 /* Packed codes: each code of V (device int32, m x n) as its `bits`-bit two's
  * complement, bits in {2, 4, 8}; code j of row i sits in byte

@@ -24,6 +24,7 @@ __all__ = [
     "quantize_host",
     "gptq",
     "quantize_range",
+    "quantize_scaled",
     "row_scales",
     "pack_codes",
     "quantize_workspace_size",
@@ -187,19 +188,54 @@ def quantize_range(W, LA, LB, scales, lo: int, hi: int, ws=None, out=None, strea
     return V, Wq, status
 
 
-def row_scales(W, lo: int, hi: int, grid: int = 1, out=None, stream=None):
+def row_scales(W, lo: int, hi: int, grid: int = 1, group: Optional[int] = None, out=None, stream=None):
     """Per-row scales of W for the alphabet {lo .. hi}, with a shrink search
     over `grid` factors from 1 down to 1/2 (bakron_row_scales).  Returns a
-    float32 CUDA tensor of m scales."""
+    float32 CUDA tensor of m scales, or of m x ceil(n / group) with a group
+    size (one scale per run of `group` columns)."""
     torch = _torch()
     lib = _lib.load()
     m, n = W.shape
     _require_cuda_f32(W, (m, n), "W")
-    scales = torch.empty(m, dtype=torch.float32, device=W.device) if out is None else out
-    _require_cuda_f32(scales, (m,), "scales")
-    st = lib.bakron_row_scales(_ptr(W), m, n, int(lo), int(hi), int(grid), _ptr(scales), _stream_handle(stream))
+    shape = (m,) if group is None else (m, -(-n // int(group)))
+    scales = torch.empty(shape, dtype=torch.float32, device=W.device) if out is None else out
+    _require_cuda_f32(scales, shape, "scales")
+    st = lib.bakron_row_scales(_ptr(W), m, n, 0 if group is None else int(group), int(lo), int(hi), int(grid),
+                               _ptr(scales), _stream_handle(stream))
     _lib.check(st, "bakron_row_scales")
     return scales
+
+
+def quantize_scaled(W, LA, LB, scales, lo: int, hi: int, group: Optional[int] = None, col_scales=None, ws=None,
+                    out=None, stream=None):
+    """quantize_range() with one scale per entry, fp32(scales[i, j // group]
+    * col_scales[j]) (bakron_quantize_scaled): `scales` holds m (group None)
+    or m x ceil(n / group) run scales, or is None; `col_scales` n column
+    scales or None.  Returns (V, Wq, status) like quantize()."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    _require_cuda_f32(LA, (n, n), "LA")
+    if LB is not None:
+        _require_cuda_f32(LB, (m, m), "LB")
+    if scales is not None:
+        _require_cuda_f32(scales, (m,) if group is None else (m, -(-n // int(group))), "scales")
+    if col_scales is not None:
+        _require_cuda_f32(col_scales, (n,), "col_scales")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, device=W.device)
+        Wq = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    else:
+        V, Wq, status = out
+    if ws is None:
+        ws = _workspace(lib.bakron_quantize_workspace_size(m, n), W.device)
+    st = lib.bakron_quantize_scaled(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), 0 if group is None else int(group),
+                                    _ptr(col_scales), int(lo), int(hi), m, n, _ptr(V), _ptr(Wq), _ptr(ws), ws.numel(),
+                                    _ptr(status), _stream_handle(stream))
+    _lib.check(st, "bakron_quantize_scaled")
+    return V, Wq, status
 
 
 def pack_codes(V, bits: int, out=None, stream=None):

@@ -43,7 +43,9 @@ SIGNATURES = {
     "bakron_gptq_workspace_size": (_sz, [_i64, _i64]),
     "bakron_gptq_quantize": (_int, [_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_range": (_int, [_vp, _vp, _vp, _vp, _int, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
-    "bakron_row_scales": (_int, [_vp, _i64, _i64, _int, _int, _int, _vp, _vp]),
+    "bakron_row_scales": (_int, [_vp, _i64, _i64, _i64, _int, _int, _int, _vp, _vp]),
+    "bakron_quantize_scaled": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _int, _int, _i64, _i64, _vp, _vp, _vp, _sz,
+                                      _vp, _vp]),
     "bakron_pack_codes": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
     "bakron_quantize_profile": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp,
                                         _vp, _vp, _vp]),

@@ -83,7 +83,7 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
     return BAKRON_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
     return BAKRON_ERR_WORKSPACE;
-  return from_cuda(bakron::quantize_launch(W, LA, LB, scales, bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
+  return from_cuda(bakron::quantize_launch(W, LA, LB, bakron::per_row(scales), bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
                                            (cudaStream_t)stream));
 }
 
@@ -99,7 +99,7 @@ int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, i
   if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
     return BAKRON_ERR_WORKSPACE;
   // L_B = I: the solver skips every column term (nullptr output factor).
-  return from_cuda(bakron::quantize_launch(W, LA, nullptr, scales, bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
+  return from_cuda(bakron::quantize_launch(W, LA, nullptr, bakron::per_row(scales), bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
                                            (cudaStream_t)stream));
 }
 
@@ -114,17 +114,36 @@ int bakron_quantize_range(const float* W, const float* LA, const float* LB, cons
     return BAKRON_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
     return BAKRON_ERR_WORKSPACE;
-  return from_cuda(bakron::quantize_launch(W, LA, LB, scales, bakron::Alphabet{true, lo, hi}, (int)m, (int)n, V, Wq,
+  return from_cuda(bakron::quantize_launch(W, LA, LB, bakron::per_row(scales), bakron::Alphabet{true, lo, hi}, (int)m, (int)n, V, Wq,
                                            ws, status_dev, (cudaStream_t)stream));
 }
 
-int bakron_row_scales(const float* W, int64_t m, int64_t n, int lo, int hi, int grid, float* scales, void* stream) {
-  if (!W || !scales || m < 1 || n < 1 || m * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+int bakron_row_scales(const float* W, int64_t m, int64_t n, int64_t group, int lo, int hi, int grid, float* scales,
+                      void* stream) {
+  if (!W || !scales || m < 1 || n < 1 || m * n >= kMaxElems || group < 0) return BAKRON_ERR_INVALID_ARG;
   if (!(lo < 0 && hi > 0 && lo >= -BAKRON_MAX_CODE && hi <= BAKRON_MAX_CODE)) return BAKRON_ERR_INVALID_ARG;
   if (grid < 1 || grid > BAKRON_MAX_SCALE_GRID) return BAKRON_ERR_INVALID_ARG;
   if ((const void*)W == (const void*)scales) return BAKRON_ERR_INVALID_ARG;
-  return from_cuda(bakron::row_scales_launch(W, (int)m, (int)n, bakron::Alphabet{true, lo, hi}, grid, scales,
+  const int g = (group == 0 || group > n) ? (int)n : (int)group;
+  return from_cuda(bakron::row_scales_launch(W, (int)m, (int)n, g, bakron::Alphabet{true, lo, hi}, grid, scales,
                                              (cudaStream_t)stream));
+}
+
+int bakron_quantize_scaled(const float* W, const float* LA, const float* LB, const float* scales, int64_t group,
+                           const float* col_scales, int lo, int hi, int64_t m, int64_t n, int32_t* V, float* Wq,
+                           void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+  if (!W || !LA || !V || !Wq || !status_dev) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems || group < 0) return BAKRON_ERR_INVALID_ARG;
+  if (!(lo < hi && lo <= 0 && hi >= 0 && lo >= -BAKRON_MAX_CODE && hi <= BAKRON_MAX_CODE))
+    return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)Wq == (const void*)W || (const void*)V == (const void*)W || (void*)V == (void*)Wq)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  const int g = (group == 0 || group > n) ? (int)n : (int)group;
+  return from_cuda(bakron::quantize_launch(W, LA, LB, bakron::Scales{scales, g, col_scales},
+                                           bakron::Alphabet{true, lo, hi}, (int)m, (int)n, V, Wq, ws, status_dev,
+                                           (cudaStream_t)stream));
 }
 
 int bakron_pack_codes(const int32_t* V, int64_t m, int64_t n, int bits, uint8_t* out, void* stream) {
@@ -146,7 +165,7 @@ int bakron_quantize_profile(const float* W, const float* LA, const float* LB, co
   if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
     return BAKRON_ERR_WORKSPACE;
   bakron::KernelTimer t;
-  cudaError_t e = bakron::quantize_launch(W, LA, LB, scales, bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
+  cudaError_t e = bakron::quantize_launch(W, LA, LB, bakron::per_row(scales), bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
                                           (cudaStream_t)stream, &t);
   if (e != cudaSuccess) return BAKRON_ERR_CUDA;
   for (int c = 0; c < bakron::kKernelClasses; ++c) {
@@ -197,7 +216,7 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
   if (e == cudaSuccess) e = cudaMemcpyAsync(dLB, LB, (size_t)m * m * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && scales) e = cudaMemcpyAsync(dS, scales, (size_t)m * 4, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return BAKRON_ERR_CUDA;
-  e = bakron::quantize_launch(dW, dLA, dLB, scales ? dS : nullptr, bakron::alphabet_from_bits(bits), (int)m, (int)n, dV, dWq, qws, dStatus,
+  e = bakron::quantize_launch(dW, dLA, dLB, bakron::per_row(scales ? dS : nullptr), bakron::alphabet_from_bits(bits), (int)m, (int)n, dV, dWq, qws, dStatus,
                               s);
   if (e != cudaSuccess) return BAKRON_ERR_CUDA;
   e = cudaMemcpyAsync(V, dV, mn * 4, cudaMemcpyDeviceToHost, s);

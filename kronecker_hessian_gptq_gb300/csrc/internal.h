@@ -30,14 +30,26 @@ inline Alphabet alphabet_from_bits(int bits) {
   return bits ? Alphabet{true, -(1 << (bits - 1)), (1 << (bits - 1)) - 1} : Alphabet{false, 0, 0};
 }
 
+// Scales of the alphabet: entry (i, j) has scale fp32(R[i][j / group] t[j]),
+// R m x ceil(n / group) (group <= 0 or >= n: one scale per row), R or t null
+// for ones.
+struct Scales {
+  const float* R;
+  int group;
+  const float* t;
+};
+inline Scales per_row(const float* s) { return Scales{s, 0, nullptr}; }
+
 // quantize.cu (LB == nullptr: the output factor is the identity, row-wise GPTQ)
 size_t quantize_workspace_bytes(int64_t m, int64_t n);
-cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
+cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Scales sc,
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
 
 // scales.cu
-cudaError_t row_scales_launch(const float* W, int m, int n, Alphabet al, int grid, float* scales,
+// One scale per run of `group` columns of each row (group <= 0 or >= n: per
+// row), m x ceil(n / group) outputs.
+cudaError_t row_scales_launch(const float* W, int m, int n, int group, Alphabet al, int grid, float* scales,
                               cudaStream_t stream);
 cudaError_t pack_codes_launch(const int32_t* V, int m, int n, int bits, uint8_t* out, cudaStream_t stream);
 

@@ -60,7 +60,7 @@ extern "C" int bakron_quantize_noalloc(const float* W, const float* LA, const fl
   if (scratch_address(&ws) != cudaSuccess) return BAKRON_ERR_CUDA;
   // The solve initializes every scratch byte it reads (status word, header
   // and state planes), so what an earlier call left there does not matter.
-  cudaError_t e = bakron::quantize_launch(W, LA, LB, scales, bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
+  cudaError_t e = bakron::quantize_launch(W, LA, LB, bakron::per_row(scales), bakron::alphabet_from_bits(bits), (int)m, (int)n, V, Wq, ws, status_dev,
                                           (cudaStream_t)stream);
   return e == cudaSuccess ? BAKRON_OK : BAKRON_ERR_CUDA;
 }

@@ -65,9 +65,10 @@ constexpr int U = 4;   // target tiles per push CTA
 
 struct Header {
   unsigned maxw_bits;  // max |W| as ordered uint bits
-  unsigned maxs_bits;  // max scale
+  unsigned maxs_bits;  // max row (or group) scale
+  unsigned maxc_bits;  // max column scale
   float sigma;         // offset of the offset accumulators
-  int pad[61];
+  int pad[60];
 };
 static_assert(sizeof(Header) == 256, "header is one alignment unit");
 
@@ -77,7 +78,9 @@ struct QParams {
   const float* W;
   const float* LA;
   const float* LB;
-  const float* scales;
+  const float* scales;   // m x ngroups row (group) scales, or null
+  const float* cscales;  // n column scales, or null
+  int group, ngroups;    // columns per scale run; runs per row
   int32_t* V;
   float* Wq;
   float2* Xm;  // column pushes from single tiles (mid)
@@ -106,7 +109,7 @@ __device__ __forceinline__ unsigned warp_max(unsigned v) {
 __global__ void prepass_kernel(QParams P) {
   const size_t total = (size_t)P.m * P.n;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  unsigned wmax = 0, smax = 0;
+  unsigned wmax = 0, smax = 0, cmax = 0;
   int bad = 0;
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
     const float w = P.W[idx];
@@ -117,7 +120,8 @@ __global__ void prepass_kernel(QParams P) {
     }
   }
   if (P.scales) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)P.m; i += stride) {
+    const size_t ns = (size_t)P.m * P.ngroups;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < ns; i += stride) {
       const float s = P.scales[i];
       if (!(s > 0.f) || !isfinite(s)) {
         bad |= BAKRON_DEV_BAD_SCALE;
@@ -126,18 +130,33 @@ __global__ void prepass_kernel(QParams P) {
       }
     }
   }
+  if (P.cscales) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)P.n; i += stride) {
+      const float t = P.cscales[i];
+      if (!(t > 0.f) || !isfinite(t)) {
+        bad |= BAKRON_DEV_BAD_SCALE;
+      } else {
+        cmax = max(cmax, __float_as_uint(t));
+      }
+    }
+  }
   wmax = warp_max(wmax);
   smax = warp_max(smax);
+  cmax = warp_max(cmax);
   if ((threadIdx.x & 31) == 0) {
     atomicMax(&P.hdr->maxw_bits, wmax);
     atomicMax(&P.hdr->maxs_bits, smax);
+    atomicMax(&P.hdr->maxc_bits, cmax);
   }
   if (bad) atomicOr(P.status, bad);
 }
 
 __global__ void sigma_kernel(QParams P) {
   const float maxw = __uint_as_float(P.hdr->maxw_bits);
-  const float maxs = P.scales ? __uint_as_float(P.hdr->maxs_bits) : 1.f;
+  // Every entry's scale is at most (max row scale) (max column scale), up to
+  // one fp32 rounding, far inside the margin below.
+  const float maxs = (P.scales ? __uint_as_float(P.hdr->maxs_bits) : 1.f) *
+                     (P.cscales ? __uint_as_float(P.hdr->maxc_bits) : 1.f);
   const float levels = P.bits ? (float)max(-P.lo, P.hi) : 1.f;
   // Every value rounded or accumulated stays within a few alphabet steps of
   // the weights; the offset leaves a wide margin above that.
@@ -306,8 +325,20 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
       for (int j = 0; j < kPer; ++j) acc[j].mac(l, sA[i][qj[j]]);
     }
   }
-  const float s = (P.scales != nullptr && vr) ? P.scales[r] : 1.f;
-  const float rcp = __frcp_rn(s);
+  // Each entry's scale: its row (group) scale times its column scale,
+  // rounded once to fp32; and its reciprocal for the rounding decision.
+  float se[kPer], rcpe[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int c = J * T + qj[j];
+    float sv = 1.f;
+    if (vr && c < P.n) {
+      if (P.scales) sv = P.scales[(size_t)r * P.ngroups + c / P.group];
+      if (P.cscales) sv = __fmul_rn(sv, P.cscales[c]);
+    }
+    se[j] = sv;
+    rcpe[j] = __frcp_rn(sv);
+  }
   const float flo = (float)P.lo, fhi = (float)P.hi;
   __syncthreads();
 #pragma unroll
@@ -347,12 +378,12 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
           // fp32 decision: x.x == fp32(x); x.x * rcp is within 2 ulp of the
           // correctly rounded quotient, which is used near a rounding tie
           // (and for an infinite or NaN product: a scale below 2^-128).
-          float y = x.x * rcp;
-          if (!(fabsf(y) <= 256.f) || fabsf(y - floorf(y) - 0.5f) < 1e-3f) y = __fdiv_rn(x.x, s);
+          float y = x.x * rcpe[j];
+          if (!(fabsf(y) <= 256.f) || fabsf(y - floorf(y) - 0.5f) < 1e-3f) y = __fdiv_rn(x.x, se[j]);
           float v = rintf(y);
           if (P.bits) v = fminf(fmaxf(v, flo), fhi);
           // e = s v - x: exact high-word difference, then the low words
-          const float2 sv = two_prod(s, v);
+          const float2 sv = two_prod(se[j], v);
           const float2 h = two_sum(sv.x, -x.x);
           const float2 e = fast_two_sum(h.x, (sv.y - x.y) + h.y);
           sB[p][q] = e;
@@ -369,7 +400,7 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
     if (vr && c < P.n) {
       const size_t o = (size_t)r * P.n + c;
       P.V[o] = (int32_t)vkeep[j];
-      P.Wq[o] = s * vkeep[j];
+      P.Wq[o] = se[j] * vkeep[j];
     }
   }
   __syncthreads();
@@ -1158,7 +1189,7 @@ WsLayout ws_layout(int64_t m, int64_t n) {
 
 size_t quantize_workspace_bytes(int64_t m, int64_t n) { return ws_layout(m, n).total; }
 
-cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, const float* scales,
+cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Scales sc,
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
   const WsLayout lay = ws_layout(m, n);
@@ -1170,7 +1201,10 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, co
   P.W = W;
   P.LA = LA;
   P.LB = LB;
-  P.scales = scales;
+  P.scales = sc.R;
+  P.cscales = sc.t;
+  P.group = (sc.group <= 0 || sc.group > n) ? n : sc.group;
+  P.ngroups = (n + P.group - 1) / P.group;
   P.V = V;
   P.Wq = Wq;
   P.hdr = reinterpret_cast<Header*>(base);

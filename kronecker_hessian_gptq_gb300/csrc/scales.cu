@@ -61,16 +61,20 @@ __device__ __forceinline__ float2 df_block_sum(float2 v, float2* red) {
   return t;  // valid in thread 0
 }
 
-// One CTA per row; the row is staged in dynamic shared memory.
-__global__ void __launch_bounds__(kScaleThreads) row_scales_kernel(const float* W, int n, int lo, int hi, int grid,
-                                                                    bool staged, ShrinkTable tab, float* scales) {
+// One CTA per run of `group` columns of a row (blockIdx.x = row * runs +
+// run); the run is staged in dynamic shared memory.
+__global__ void __launch_bounds__(kScaleThreads) row_scales_kernel(const float* W, int n, int group, int runs, int lo,
+                                                                    int hi, int grid, bool staged, ShrinkTable tab,
+                                                                    float* scales) {
   extern __shared__ float srow[];
   __shared__ float2 red[kScaleThreads / 32];
   __shared__ float smax[kScaleThreads / 32];
-  const float* w = W + (size_t)blockIdx.x * n;
+  const int row = blockIdx.x / runs, run = blockIdx.x % runs;
+  const float* w = W + (size_t)row * n + (size_t)run * group;
+  const int len = min(group, n - run * group);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float mx = 0.f;
-  for (int j = threadIdx.x; j < n; j += kScaleThreads) {
+  for (int j = threadIdx.x; j < len; j += kScaleThreads) {
     const float x = w[j];
     if (staged) srow[j] = x;
     mx = fmaxf(mx, fabsf(x));
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kScaleThreads) row_scales_kernel(const float* 
     const float rcp = __frcp_rn(s);
     const float sk = scale_pow2(s, k);
     float2 acc = make_float2(0.f, 0.f);
-    for (int j = threadIdx.x; j < n; j += kScaleThreads) {
+    for (int j = threadIdx.x; j < len; j += kScaleThreads) {
       const float x = src[j];
       const float v = fminf(fmaxf(rne_quotient(x, s, rcp), flo), fhi);  // the decision on the unscaled row
       const float2 sv = two_prod(sk, v);               // s v 2^k exactly
@@ -144,18 +148,21 @@ __global__ void pack_codes_kernel(const int32_t* V, int m, int n, int bits, int 
 
 }  // namespace
 
-cudaError_t row_scales_launch(const float* W, int m, int n, Alphabet al, int grid, float* scales,
+cudaError_t row_scales_launch(const float* W, int m, int n, int group, Alphabet al, int grid, float* scales,
                               cudaStream_t stream) {
+  if (group <= 0 || group > n) group = n;
+  const int runs = (n + group - 1) / group;
   ShrinkTable tab;
   for (int g = 0; g < kMaxGrid; ++g)
     tab.f[g] = g < grid ? (grid > 1 ? (float)(1.0 - (double)g / (2.0 * (grid - 1))) : 1.f) : 0.f;
-  const bool staged = (size_t)n * sizeof(float) <= kMaxStagedBytes;
-  const size_t smem = staged ? (size_t)n * sizeof(float) : 0;
+  const bool staged = (size_t)group * sizeof(float) <= kMaxStagedBytes;
+  const size_t smem = staged ? (size_t)group * sizeof(float) : 0;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(row_scales_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  row_scales_kernel<<<m, kScaleThreads, smem, stream>>>(W, n, al.lo, al.hi, grid, staged, tab, scales);
+  row_scales_kernel<<<(unsigned)((size_t)m * runs), kScaleThreads, smem, stream>>>(W, n, group, runs, al.lo, al.hi,
+                                                                                  grid, staged, tab, scales);
   return cudaGetLastError();
 }
 

@@ -134,13 +134,19 @@ def test_range_scales_and_pack_entry_points_reject_bad_arguments(lib):
     assert q(W, W, None, None, -8, 7, 8, 8, V, V, ws, big, W, None) == 1  # V aliases Wq
     assert q(W, W, None, None, -8, 7, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
     r = lib.bakron_row_scales
-    assert r(W, 0, 8, -8, 7, 1, S, None) == 1  # m < 1
-    assert r(W, 8, 8, 0, 7, 1, S, None) == 1  # lo must be negative
-    assert r(W, 8, 8, -8, 0, 1, S, None) == 1  # hi must be positive
-    assert r(W, 8, 8, -8, 7, 0, S, None) == 1  # grid < 1
-    assert r(W, 8, 8, -8, 7, 257, S, None) == 1  # grid above the table
-    assert r(W, 8, 8, -8, 7, 4, W, None) == 1  # scales alias W
-    assert r(None, 8, 8, -8, 7, 4, S, None) == 1  # null W
+    assert r(W, 0, 8, 0, -8, 7, 1, S, None) == 1  # m < 1
+    assert r(W, 8, 8, -1, -8, 7, 1, S, None) == 1  # negative group
+    assert r(W, 8, 8, 0, 0, 7, 1, S, None) == 1  # lo must be negative
+    assert r(W, 8, 8, 0, -8, 0, 1, S, None) == 1  # hi must be positive
+    assert r(W, 8, 8, 0, -8, 7, 0, S, None) == 1  # grid < 1
+    assert r(W, 8, 8, 0, -8, 7, 257, S, None) == 1  # grid above the table
+    assert r(W, 8, 8, 0, -8, 7, 4, W, None) == 1  # scales alias W
+    assert r(None, 8, 8, 0, -8, 7, 4, S, None) == 1  # null W
+    qs = lib.bakron_quantize_scaled
+    assert qs(W, W, None, S, -1, None, -8, 7, 8, 8, V, Wq, ws, big, W, None) == 1  # negative group
+    assert qs(W, W, None, S, 2, S, 7, -8, 8, 8, V, Wq, ws, big, W, None) == 1  # lo > hi
+    assert qs(W, W, None, S, 2, S, -8, 7, 8, 8, W, Wq, ws, big, W, None) == 1  # V aliases W
+    assert qs(W, W, None, S, 2, S, -8, 7, 8, 8, V, Wq, ws, big - 1, W, None) == 4  # small workspace
     p = lib.bakron_pack_codes
     assert p(V, 8, 8, 3, S, None) == 1  # bits not in {2, 4, 8}
     assert p(V, 8, 0, 4, S, None) == 1  # n < 1

@@ -220,3 +220,104 @@ def test_scales_solve_pack_end_to_end(bk):
     Vg = V.cpu().numpy()
     assert O.match_fraction(Vg, Vo) >= V_MATCH
     assert np.array_equal(P.cpu().numpy(), O.pack_codes(Vg, 4))
+
+
+@pytest.mark.parametrize("m,n,group", [(5, 9, 4), (64, 1000, 128), (20, 300, 300), (3, 70000, 60001)])
+def test_grouped_scales_against_oracle(bk, m, n, group):
+    """One scale per run of `group` columns; each run checked like a row."""
+    import torch
+
+    rng = np.random.default_rng(m + n + group)
+    W = rng.standard_normal((m, n)).astype(np.float32)
+    W[:, ::97] *= 6.0
+    Sg = bk.row_scales(_dev(W), -4, 3, 16, group=group)
+    torch.cuda.synchronize()
+    Sg = Sg.cpu().numpy()
+    runs = -(-n // group)
+    assert Sg.shape == (m, runs)
+    for k in range(runs):
+        _check_scales(W[:, k * group:(k + 1) * group], -4, 3, 16, Sg[:, k])
+
+
+def _scaled_case(m, n, group, with_cols, seed):
+    p = random_problem(m, n, bits=0, seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    R = None
+    if group is not None or not with_cols:
+        R, _ = O.row_scales(p.W, -7, 7, 8, group=group)
+    t = rng.uniform(0.5, 2.0, n).astype(np.float32) if with_cols else None
+    S = O.element_scales(np.ones(m, np.float32) if R is None else R, n, group=group, col_scales=t)
+    return p, R, t, S
+
+
+@pytest.mark.parametrize("m,n", [(5, 3), (45, 70), (130, 257)])
+@pytest.mark.parametrize("group,with_cols", [(32, False), (16, True), (None, True), (100, True)])
+@pytest.mark.parametrize("with_lb", [True, False])
+def test_quantize_scaled_against_oracle(bk, m, n, group, with_cols, with_lb):
+    import torch
+
+    p, R, t, S = _scaled_case(m, n, group, with_cols, seed=m * 13 + n + (group or 0))
+    LA, LB, info = bk.prepare(_dev(p.A), _dev(p.B))
+    assert info.cpu().tolist() == [0, 0]
+    V, Wq, st = bk.quantize_scaled(_dev(p.W), LA, LB if with_lb else None, _dev(R), -7, 7, group=group,
+                                   col_scales=_dev(t))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    V = V.cpu().numpy().astype(np.int64)
+    Wq = Wq.cpu().numpy()
+    assert np.array_equal(Wq, (S * V.astype(np.float32)).astype(np.float32))
+    if with_lb:
+        LA64, LB64 = O.factors_of(p.A, p.B)
+        Vo, Wqo, _ = O.bakron(p.W, LA=LA64, LB=LB64, scales=S, bits=(-7, 7))
+        Bm = p.B
+    else:
+        Vo, Wqo, _ = O.gptq_rows(p.W, p.A, S, (-7, 7))
+        Bm = np.eye(m)
+    assert O.match_fraction(V, Vo) >= V_MATCH
+    d_ref = O.distortion(p.W, Wqo, p.A, Bm)
+    d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, Bm)
+    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+
+
+def test_quantize_scaled_defaults_equal_range(bk):
+    """No groups and no column scales is bakron_quantize_range bit for bit."""
+    import torch
+
+    p = random_problem(70, 90, bits=4, seed=29)
+    LA, LB, _ = bk.prepare(_dev(p.A), _dev(p.B))
+    V1, Wq1, s1 = bk.quantize_range(_dev(p.W), LA, LB, _dev(p.scales), -8, 7)
+    V2, Wq2, s2 = bk.quantize_scaled(_dev(p.W), LA, LB, _dev(p.scales), -8, 7)
+    torch.cuda.synchronize()
+    assert int(s1.item()) == 0 and int(s2.item()) == 0
+    assert torch.equal(V1, V2) and torch.equal(Wq1, Wq2)
+
+
+def test_quantize_scaled_rejects_bad_column_scales(bk):
+    import torch
+
+    p = random_problem(20, 30, bits=4, seed=2)
+    LA, LB, _ = bk.prepare(_dev(p.A), _dev(p.B))
+    t = np.ones(30, np.float32)
+    t[7] = 0.0
+    _, _, st = bk.quantize_scaled(_dev(p.W), LA, LB, _dev(p.scales), -8, 7, col_scales=_dev(t))
+    torch.cuda.synchronize()
+    assert int(st.item()) & 2  # BAKRON_DEV_BAD_SCALE
+
+
+def test_quantize_scaled_multi_tile_grouped(bk):
+    """Groups of 128 and column scales over many tiles and chunks (520 x 700,
+    ragged in both dimensions), BaKron with both factors."""
+    import torch
+
+    p, R, t, S = _scaled_case(520, 700, 128, True, seed=77)
+    LA, LB, _ = bk.prepare(_dev(p.A), _dev(p.B))
+    V, Wq, st = bk.quantize_scaled(_dev(p.W), LA, LB, _dev(R), -7, 7, group=128, col_scales=_dev(t))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    LA64, LB64 = O.factors_of(p.A, p.B)
+    Vo, Wqo, _ = O.bakron(p.W, LA=LA64, LB=LB64, scales=S, bits=(-7, 7))
+    V = V.cpu().numpy().astype(np.int64)
+    assert O.match_fraction(V, Vo) >= V_MATCH
+    d_ref = O.distortion(p.W, Wqo, p.A, p.B)
+    d_gpu = O.distortion(p.W, Wq.cpu().numpy().astype(np.float64), p.A, p.B)
+    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
