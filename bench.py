@@ -248,6 +248,140 @@ def profiled_traffic(kernel: str, workload: str):
     return int(b.group(1))
 
 
+# fp32 operations of one candidate evaluation in the scale search (counted
+# from csrc/scales.cu: quotient and tie test 8, clamp 2, power-of-two scaling
+# 2, exact error 15, its square 4, double-float accumulation 20).
+SCALE_OPS_PER_EVAL = 51
+
+
+def run_scales(args, p, W, LA, LB, s, ws, out, flush, world, dev):
+    """The base quantizer's side kernels on the layer: the App. D scale search
+    (grid `--scale-grid` shrink factors, alphabet {-2^(b-1) .. 2^(b-1)-1}) and
+    the packing of the layer's codes to b bits; one step = both kernels."""
+    import torch
+
+    import kronecker_hessian_gptq_gb300 as bk
+
+    m, n, bits = p.m, p.n, p.bits
+    lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
+    V = bk.quantize(W, LA, LB, s, bits, ws=ws, out=out)[0]
+    S = torch.empty(m, dtype=torch.float32, device=dev)
+    P = torch.empty((m, (n * bits + 7) // 8), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        bk.row_scales(W, lo, hi, args.scale_grid, out=S)
+        bk.pack_codes(V, bits, out=P)
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier(world, dev)
+    marks = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    for a, b, c in marks:
+        flush.zero_()
+        a.record()
+        bk.row_scales(W, lo, hi, args.scale_grid, out=S)
+        b.record()
+        bk.pack_codes(V, bits, out=P)
+        c.record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    clocks = sampler.stop()
+    scale_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / args.steps
+    pack_ms = sum(b.elapsed_time(c) for _, b, c in marks) / args.steps
+    total_ms = aggregate_max(sum(a.elapsed_time(c) for a, _, c in marks), world, dev)
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = SM_COUNT * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12  # T fp32 lane operations / s
+    achieved = m * n * args.scale_grid * SCALE_OPS_PER_EVAL / (scale_ms * 1e-3) / 1e12
+    pack_bytes = 4 * m * n + m * ((n * bits + 7) // 8)
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    cfg = workload_config(p, world)
+    cfg["method"] = f"scale search ({args.scale_grid} shrink factors) + {bits}-bit packing"
+    return {
+        "metric": "scale search + code packing, weights/s per m x n layer", "unit": UNIT,
+        "value": world * m * n * args.steps / (total_ms * 1e-3), "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 decisions, f32x2 error sums; int32 -> packed bits", "data": "synthetic",
+        "config": cfg, "clocks": clocks, "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "alu", "kernel": "row_scales", "achieved": achieved, "peak": alu_peak,
+                     "unit": "T fp32 ops/s", "frac": achieved / alu_peak, "traffic": None,
+                     "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_max:.0f} MHz; "
+                                   f"{SCALE_OPS_PER_EVAL} ops per candidate evaluation"},
+        "kernels": {"row_scales": {"ms": scale_ms},
+                    "pack_codes": {"ms": pack_ms, "bound": "hbm", "bytes": pack_bytes,
+                                   "achieved_gbs": pack_bytes / (pack_ms * 1e-3) / 1e9, "peak_gbs": hbm,
+                                   "frac": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm}},
+        "e2e": None,
+    }
+
+
+def antidiag_macs(m: int, n: int) -> int:
+    """Multiply-adds of Algorithm 3 with triangular factors: entry (p, q)
+    receives one per earlier entry (i, j) with i <= p, j <= q."""
+    return (m * (m + 1) // 2) * (n * (n + 1) // 2) - m * n
+
+
+def run_antidiag(args, p, W, LA, LB, s, ws, out, flush, world, dev):
+    """BaKron-antidiagonal (Algorithm 3) on the layer, and the BaKron solve
+    on the same inputs: the pages' speedup column (Table 3) on this GPU."""
+    import torch
+
+    import kronecker_hessian_gptq_gb300 as bk
+
+    m, n = p.m, p.n
+    ws_ad = torch.empty(bk.load_library().bakron_antidiag_workspace_size(m, n), dtype=torch.uint8, device=dev)
+    out_ad = (torch.empty((m, n), dtype=torch.int32, device=dev), torch.empty((m, n), dtype=torch.float32, device=dev),
+              torch.zeros(1, dtype=torch.int32, device=dev))
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def timed(fn, steps):
+        marks = [(ev(), ev()) for _ in range(steps)]
+        for a, b in marks:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in marks)
+
+    solve_ad = lambda: bk.antidiag(W, LA, LB, s, p.bits, ws=ws_ad, out=out_ad)  # noqa: E731
+    solve_bk = lambda: bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        solve_ad()
+        solve_bk()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier(world, dev)
+    ad_ms = aggregate_max(timed(solve_ad, args.steps), world, dev)
+    barrier(world, dev)
+    clocks = sampler.stop()
+    bk_ms = aggregate_max(timed(solve_bk, args.steps), world, dev)
+    if out_ad[2].item() != 0 or out[2].item() != 0:
+        raise RuntimeError(f"device status {out_ad[2].item()} / {out[2].item()}")
+    same = float((out_ad[0] == out[0]).float().mean().item())
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    alg = 2.0 * antidiag_macs(m, n) / (ad_ms / args.steps * 1e-3) / 1e12
+    peak = alu_peak_tflops(sm_max)
+    cfg = workload_config(p, world)
+    cfg["method"] = "BaKron-antidiagonal (Algorithm 3), double-float"
+    return {
+        "metric": "BaKron-antidiagonal solve time & weights quantized/s per m x n layer", "unit": UNIT,
+        "value": world * m * n * args.steps / (ad_ms * 1e-3), "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ad_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32x2 double-float", "data": "synthetic", "config": cfg, "clocks": clocks,
+        "gpu_launches": (m + n + 1) * args.steps,
+        "bakron_ms_per_step": bk_ms / args.steps, "speedup_bakron_over_antidiag": ad_ms / bk_ms,
+        "codes_identical_fraction": same,
+        "roofline": {"bound": "alu", "kernel": "ad_step", "achieved": alg, "peak": peak, "unit": "TFLOP/s",
+                     "frac": alg / peak, "traffic": None, "alg_macs": antidiag_macs(m, n),
+                     "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} fp32 lanes x {sm_max:.0f} MHz / "
+                                   f"{DF_INSTR_PER_MAC} instr per double-float MAC x 2 flops"},
+        "e2e": None,
+    }
+
+
 def run_ours(args, rank, local_rank, world):
     import ctypes
 
@@ -280,6 +414,10 @@ def run_ours(args, rank, local_rank, world):
     out = (torch.empty((m, n), dtype=torch.int32, device=dev), torch.empty((m, n), dtype=torch.float32, device=dev),
            torch.zeros(1, dtype=torch.int32, device=dev))
     flush = torch.empty((512 << 20) // 4, dtype=torch.float32, device=dev)
+    if args.method == "scales":
+        return run_scales(args, p, W, LA, LB, s, ws, out, flush, world, dev)
+    if args.method == "antidiag":
+        return run_antidiag(args, p, W, LA, LB, s, ws, out, flush, world, dev)
     if args.method == "gptq":  # row-wise GPTQ: the one-sided case B = I of the same solve
         solve = lambda: bk.gptq(W, LA, s, p.bits, ws=ws, out=out)  # noqa: E731
     else:
@@ -390,8 +528,11 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq"],
-                    help="bakron (default, the headline) or gptq: row-wise GPTQ, the case B = I")
+    ap.add_argument("--scale-grid", type=int, default=100, help="shrink factors of --method scales")
+    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq", "scales", "antidiag"],
+                    help="bakron (default, the headline); gptq: row-wise GPTQ, the case B = I; scales: the "
+                         "scale search and code packing kernels; antidiag: Algorithm 3 beside BaKron "
+                         "(give --config c2 for a short run)")
     args = ap.parse_args(argv)
     rank, local_rank, world = dist_env()
     if world > 1:

@@ -151,6 +151,24 @@ size_t bakron_gptq_workspace_size(int64_t m, int64_t n);
 int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, int bits, int64_t m, int64_t n,
                          int32_t* V, float* Wq, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
 
+/* ------------------------------------------------- BaKron-antidiagonal
+ * Algorithm 3 of "BaKron: Efficient Quantization with Kronecker-Factored
+ * Hessians" (Sec. 3.2; the BaKron-antidiag. column of Table 3, equivalent to
+ * the iterative YAQA): the anti-diagonals are rounded in order, and after
+ * each the errors of the whole anti-diagonal update every later entry,
+ *     W~ += L_B Delta L_A^T      (Delta nonzero on one anti-diagonal),
+ * m + n - 1 steps and about m^2 n^2 / 4 multiply-adds in all -- the
+ * quartic-work baseline BaKron improves on.  Same rounding, arithmetic
+ * (double-float) and codes as bakron_quantize (Theorem 3.2), one kernel
+ * launch per anti-diagonal on `stream`.  Arguments, results and errors as
+ * bakron_quantize; workspace bakron_antidiag_workspace_size(m, n) bytes
+ * (8 bytes per weight plus 16 per row).
+ */
+size_t bakron_antidiag_workspace_size(int64_t m, int64_t n);
+int bakron_antidiag_quantize(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                             int32_t* status_dev, void* stream);
+
 /* -------------------------------------------- alphabets, scales, packing
  * The base quantizer's variants ("BaKron: Efficient Quantization with
  * Kronecker-Factored Hessians", App. D: per-output-feature scales from the

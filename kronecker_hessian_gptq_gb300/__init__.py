@@ -23,6 +23,7 @@ __all__ = [
     "quantize",
     "quantize_host",
     "gptq",
+    "antidiag",
     "quantize_range",
     "quantize_scaled",
     "row_scales",
@@ -158,6 +159,32 @@ def gptq(W, LA, scales=None, bits: int = 0, ws=None, out=None, stream=None):
     st = lib.bakron_gptq_quantize(_ptr(W), _ptr(LA), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq), _ptr(ws),
                                   ws.numel(), _ptr(status), _stream_handle(stream))
     _lib.check(st, "bakron_gptq_quantize")
+    return V, Wq, status
+
+
+def antidiag(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=None):
+    """BaKron-antidiagonal (Algorithm 3, bakron_antidiag_quantize): the same
+    codes as quantize() by Theorem 3.2, with O(m^2 n^2) work in m + n - 1
+    launches.  Returns (V, Wq, status) like quantize()."""
+    torch = _torch()
+    lib = _lib.load()
+    m, n = W.shape
+    _require_cuda_f32(W, (m, n), "W")
+    _require_cuda_f32(LA, (n, n), "LA")
+    _require_cuda_f32(LB, (m, m), "LB")
+    if scales is not None:
+        _require_cuda_f32(scales, (m,), "scales")
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.int32, device=W.device)
+        Wq = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    else:
+        V, Wq, status = out
+    if ws is None:
+        ws = _workspace(lib.bakron_antidiag_workspace_size(m, n), W.device)
+    st = lib.bakron_antidiag_quantize(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
+                                      _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
+    _lib.check(st, "bakron_antidiag_quantize")
     return V, Wq, status
 
 

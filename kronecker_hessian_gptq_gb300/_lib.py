@@ -47,6 +47,8 @@ SIGNATURES = {
     "bakron_quantize_scaled": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _int, _int, _i64, _i64, _vp, _vp, _vp, _sz,
                                       _vp, _vp]),
     "bakron_pack_codes": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
+    "bakron_antidiag_workspace_size": (_sz, [_i64, _i64]),
+    "bakron_antidiag_quantize": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_profile": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp,
                                         _vp, _vp, _vp]),
     "bakron_quantize_host_workspace_size": (_sz, [_i64, _i64]),

@@ -152,6 +152,25 @@ int bakron_pack_codes(const int32_t* V, int64_t m, int64_t n, int bits, uint8_t*
   return from_cuda(bakron::pack_codes_launch(V, (int)m, (int)n, bits, out, (cudaStream_t)stream));
 }
 
+size_t bakron_antidiag_workspace_size(int64_t m, int64_t n) {
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return 0;
+  return bakron::antidiag_workspace_bytes(m, n);
+}
+
+int bakron_antidiag_quantize(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                             int32_t* status_dev, void* stream) {
+  if (!W || !LA || !LB || !V || !Wq || !status_dev) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if (!(bits == 0 || (bits >= 2 && bits <= 8))) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)Wq == (const void*)W || (const void*)V == (const void*)W || (void*)V == (void*)Wq)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::antidiag_workspace_bytes(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  return from_cuda(bakron::antidiag_launch(W, LA, LB, scales, bakron::alphabet_from_bits(bits), (int)m, (int)n, V,
+                                           Wq, ws, status_dev, (cudaStream_t)stream));
+}
+
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,

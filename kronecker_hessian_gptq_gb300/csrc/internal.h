@@ -46,6 +46,12 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
 
+// antidiag.cu (Algorithm 3, one launch per anti-diagonal; per-row scales)
+size_t antidiag_workspace_bytes(int64_t m, int64_t n);
+cudaError_t antidiag_launch(const float* W, const float* LA, const float* LB, const float* scales, Alphabet al,
+                            int m, int n, int32_t* V, float* Wq, void* ws, int32_t* status_dev,
+                            cudaStream_t stream);
+
 // scales.cu
 // One scale per run of `group` columns of each row (group <= 0 or >= n: per
 // row), m x ceil(n / group) outputs.

@@ -152,3 +152,19 @@ def test_range_scales_and_pack_entry_points_reject_bad_arguments(lib):
     assert p(V, 8, 0, 4, S, None) == 1  # n < 1
     assert p(None, 8, 8, 4, S, None) == 1  # null V
     assert p(V, 8, 8, 4, None, None) == 1  # null out
+
+
+def test_antidiag_entry_point_rejects_bad_arguments(lib):
+    W = ctypes.c_void_p(0x1000)
+    V, Wq = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    ws = ctypes.c_void_p(0x100000)
+    need = lib.bakron_antidiag_workspace_size(8, 8)
+    assert need == 512 + 256  # 8 x 8 double-float W~, two error rows (each padded to 256 bytes)
+    assert lib.bakron_antidiag_workspace_size(0, 8) == 0
+    a = lib.bakron_antidiag_quantize
+    assert a(W, W, W, None, 4, 0, 8, V, Wq, ws, need, W, None) == 1  # m < 1
+    assert a(W, W, None, None, 4, 8, 8, V, Wq, ws, need, W, None) == 1  # null LB
+    assert a(W, W, W, None, 1, 8, 8, V, Wq, ws, need, W, None) == 1  # bits
+    assert a(W, W, W, None, 4, 8, 8, V, V, ws, need, W, None) == 1  # V aliases Wq
+    assert a(W, W, W, None, 4, 8, 8, V, Wq, ws, need - 1, W, None) == 4  # small workspace
+    assert a(W, W, W, None, 4, 8, 8, V, Wq, ctypes.c_void_p(0x100010), need, W, None) == 4  # misaligned
