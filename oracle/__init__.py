@@ -46,6 +46,13 @@ What is here, and what pins it (the pins live in ``tests/test_oracle_*.py``):
       scale) and the no-search case.
   scales.pack_codes / unpack_codes  b-bit two's complement packing.  Pinned
       by hand-packed bytes (tests/golden/pack_codes.json) and round trips.
+  hessian.weighted_gram / kfac_factors / shampoo_factors / damp
+      Kronecker factors from samples (Sec. 4.2, App. A.2, App. D damping).
+      Pinned by hand-worked values (tests/golden/hessian.json), closed forms
+      (orthogonal rows, single samples, a fixed output side), and the
+      Van Loan-Pitsianis rearrangement of the explicit Kronecker sum: one
+      Shampoo step is R(H) applied to the identity, many converge to the top
+      singular pair.
   scales.element_scales             one scale per entry from per-row or
       per-run (group) scales and optional column scales (Sec. 3.1).  Pinned
       by hand-worked matrices; every solver accepts an m x n scale matrix,
@@ -64,6 +71,7 @@ then formed in float64 from the float64 value x.
 
 from .factors import normalized_inv_cholesky, rev_cholesky  # noqa: F401
 from .quantizer import alphabet_bounds, quantize  # noqa: F401
+from .hessian import damp, kfac_factors, shampoo_factors, squared_norms, weighted_gram  # noqa: F401
 from .scales import element_scales, pack_codes, row_error, row_scales, shrink_factors, unpack_codes  # noqa: F401
 from .naive import bakron_naive, babai_nearest_plane, gptq_rows  # noqa: F401
 from .antidiag import bakron_antidiagonal, bakron_definition  # noqa: F401

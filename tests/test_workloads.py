@@ -33,3 +33,20 @@ def test_random_problem_kinds(kind):
     assert p.W.shape == (7, 5) and p.A.shape == (5, 5) and p.B.shape == (7, 7)
     assert np.linalg.eigvalsh(p.A.astype(np.float64)).min() > 0
     assert np.linalg.eigvalsh(p.B.astype(np.float64)).min() > 0
+
+
+def test_bf16_encoding_rounds_to_nearest_even():
+    from workloads.activations import from_bf16_bits, to_bf16_bits
+
+    x = np.array([1.0, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -9, 1 + 2.0 ** -7 + 2.0 ** -8, -2.5, 0.0], np.float32)
+    y = from_bf16_bits(to_bf16_bits(x))
+    assert np.array_equal(y, np.array([1.0, 1.0, 1 + 2.0 ** -7, 1 + 2.0 ** -6, -2.5, 0.0], np.float32))
+
+
+def test_samples_are_seeded_and_bf16_valued():
+    from workloads.activations import from_bf16_bits, make_samples, to_bf16_bits
+
+    s1, s2 = make_samples(6, 4, 9, seed=3), make_samples(6, 4, 9, seed=3)
+    assert np.array_equal(s1.a_bits, s2.a_bits) and np.array_equal(s1.b_bits, s2.b_bits)
+    assert np.array_equal(to_bf16_bits(s1.a_f32), s1.a_bits)
+    assert s1.a_bits.shape == (6, 9) and s1.b_bits.shape == (4, 9)
