@@ -215,7 +215,8 @@ def measured_peaks() -> dict:
         return {}
 
 
-KERNEL_SOURCES = ("kronecker_hessian_gptq_gb300/csrc/quantize.cu", "kronecker_hessian_gptq_gb300/csrc/df.cuh")
+KERNEL_SOURCES = ("kronecker_hessian_gptq_gb300/csrc/quantize.cu", "kronecker_hessian_gptq_gb300/csrc/df.cuh",
+                  "kronecker_hessian_gptq_gb300/csrc/tc.cuh")
 
 
 def kernel_source_digest() -> str:
@@ -315,6 +316,79 @@ def run_scales(args, p, W, LA, LB, s, ws, out, flush, world, dev):
     }
 
 
+def run_gram(args, world, dev):
+    """Kronecker-factor accumulation (Sec. 4.2): the K-FAC Gram E[a a^T] and
+    the one-step Shampoo Gram E[|b|^2 a a^T] of the 4096-feature input side
+    from 65536 bf16 samples, on the tensor cores."""
+    import numpy as np
+    import torch
+
+    import kronecker_hessian_gptq_gb300 as bk
+    from workloads.activations import make_sample_config
+
+    s = make_sample_config(args.config if args.config.startswith("g") else "g3")
+    d, N = s.n, s.N
+    Xh = torch.from_numpy(s.a_bits.view(np.int16)).view(torch.bfloat16)
+    X = Xh.to(dev)
+    w = bk.sq_norms(torch.from_numpy(s.b_bits.view(np.int16)).view(torch.bfloat16).to(dev))
+    G = torch.empty((d, d), dtype=torch.float32, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        marks = [(ev(), ev()) for _ in range(args.steps)]
+        for a, b in marks:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in marks) / args.steps
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier(world, dev)
+    kfac_ms = timed(lambda: bk.gram(X, out=G))
+    shampoo_ms = timed(lambda: bk.gram(X, w, out=G))
+    barrier(world, dev)
+    clocks = sampler.stop()
+    kfac_ms = aggregate_max(kfac_ms * args.steps, world, dev) / args.steps
+    # End to end: pinned host samples in, the factor out.
+    Xp = Xh.pin_memory()
+    Gh = torch.empty((d, d), dtype=torch.float32, pin_memory=True)
+    t_e2e = []
+    for _ in range(max(1, args.steps // 2)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        Xd = Xp.to(dev, non_blocking=True)
+        bk.gram(Xd, out=G)
+        Gh.copy_(G, non_blocking=True)
+        torch.cuda.synchronize()
+        t_e2e.append(time.perf_counter() - t0)
+    e2e_s = aggregate_max(min(t_e2e), world, dev)
+    flops = float(d) * (d + 1) * N  # d(d+1)/2 distinct entries, 2N flops each
+    peaks = measured_peaks()
+    peak = float(peaks["bf16_tflops"]) if "bf16_tflops" in peaks else BF16_FALLBACK_TFLOPS
+    achieved = flops / (kfac_ms * 1e-3) / 1e12
+    return {
+        "metric": "Kronecker-factor accumulation (K-FAC Gram) TFLOP/s", "unit": "TFLOP/s",
+        "value": world * achieved, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": kfac_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 samples, fp32 accumulation", "data": "synthetic",
+        "config": {"workload": f"{s.name}: {d} features x {N} samples, Student-t (nu = 4)", "d": d, "N": N,
+                   "l2": f"inputs ({d * N * 2 / 2**20:.0f} MiB) larger than L2"},
+        "shampoo_ms": shampoo_ms, "shampoo_tflops": flops / (shampoo_ms * 1e-3) / 1e12,
+        "clocks": clocks, "gpu_launches": 2 * (args.warmup + args.steps),
+        "roofline": {"bound": "tensor", "kernel": "gram_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_basis": ("measured" if "bf16_tflops" in peaks else "fallback")
+                                   + " bf16 dense burst peak; algorithmic flops d (d + 1) N"},
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": d * N * 2,
+                "d2h_bytes_per_step": d * d * 4},
+    }
+
+
 def antidiag_macs(m: int, n: int) -> int:
     """Multiply-adds of Algorithm 3 with triangular factors: entry (p, q)
     receives one per earlier entry (i, j) with i <= p, j <= q."""
@@ -394,6 +468,8 @@ def run_ours(args, rank, local_rank, world):
     lib = bk.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    if args.method == "gram":
+        return run_gram(args, world, dev)
     p = load_workload(args.config)
     m, n = p.m, p.n
     A, B, W = (torch.from_numpy(x).to(dev) for x in (p.A, p.B, p.W))
@@ -529,10 +605,10 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-grid", type=int, default=100, help="shrink factors of --method scales")
-    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq", "scales", "antidiag"],
+    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq", "scales", "antidiag", "gram"],
                     help="bakron (default, the headline); gptq: row-wise GPTQ, the case B = I; scales: the "
                          "scale search and code packing kernels; antidiag: Algorithm 3 beside BaKron "
-                         "(give --config c2 for a short run)")
+                         "(give --config c2 for a short run); gram: Kronecker-factor accumulation")
     args = ap.parse_args(argv)
     rank, local_rank, world = dist_env()
     if world > 1:

@@ -151,6 +151,43 @@ size_t bakron_gptq_workspace_size(int64_t m, int64_t n);
 int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, int bits, int64_t m, int64_t n,
                          int32_t* V, float* Wq, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
 
+/* ------------------------------------------------ Hessian factor samples
+ * Kronecker factors of a Hessian H = E[a a^T (x) b b^T] from calibration
+ * samples ("BaKron: Efficient Quantization with Kronecker-Factored
+ * Hessians", Sec. 4.2, App. A.2, App. D):
+ *   K-FAC style      A = E[a a^T],          B = E[b b^T];
+ *   Shampoo, one power-iteration step from the identity
+ *                    A = E[|b|^2 a a^T],    B = E[|a|^2 b b^T];
+ *   damping          G + 0.5 mean(diag G) I   (App. D's regularization).
+ * Samples are bfloat16 columns, stored feature-major: X is d x N (features
+ * x samples), row i at X + i * ldx.  An expectation over several batches of
+ * samples is accumulated with beta = 1 and alpha = 1 / (total samples).
+ */
+
+/* G <- beta G + alpha X diag(w) X^T on the tensor cores (tcgen05; every
+ * bf16 product exact, fp32 accumulation over the samples).
+ * X: device, bf16 bit patterns, d x ldx, 16-byte aligned, ldx >= N and a
+ *    multiple of 8.
+ * w: device, N fp32 per-sample weights, 16-byte aligned, or NULL for ones.
+ *    With weights, w_t x_t is split into two bf16 terms (about 2^-17
+ *    relative remains) and multiplied in two products.
+ * G: device, d x d fp32, written in full (both triangles, symmetric); with
+ *    beta != 0 it must be symmetric on entry.  Not aliasing X.
+ * status_dev: device int32, set to 0 or BAKRON_DEV_TIMEOUT.
+ * d, N >= 1, d * d < 2^31.  One CTA per 128 x 128 tile of the lower block
+ * triangle, enqueued on `stream`.
+ */
+int bakron_gram(const void* X, int64_t d, int64_t N, int64_t ldx, const float* w, float alpha, float beta, float* G,
+                int32_t* status_dev, void* stream);
+
+/* w[t] = |y_t|^2 for the columns of Y (device, bf16, m x ldy, ldy >= N): the
+ * weights of one Shampoo step (squares exact, sums in double-float). */
+int bakron_sq_norms(const void* Y, int64_t m, int64_t N, int64_t ldy, float* w, void* stream);
+
+/* G <- G + rel * mean(diag G) * I in place (device, d x d fp32; App. D uses
+ * rel = 0.5).  One CTA; the trace is summed in double-float. */
+int bakron_damp(float* G, int64_t d, float rel, void* stream);
+
 /* ------------------------------------------------- BaKron-antidiagonal
  * Algorithm 3 of "BaKron: Efficient Quantization with Kronecker-Factored
  * Hessians" (Sec. 3.2; the BaKron-antidiag. column of Table 3, equivalent to

@@ -24,6 +24,9 @@ __all__ = [
     "quantize_host",
     "gptq",
     "antidiag",
+    "gram",
+    "sq_norms",
+    "damp",
     "quantize_range",
     "quantize_scaled",
     "row_scales",
@@ -186,6 +189,55 @@ def antidiag(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=No
                                       _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
     _lib.check(st, "bakron_antidiag_quantize")
     return V, Wq, status
+
+
+def _require_bf16_rows(X, name):
+    torch = _torch()
+    if not (X.is_cuda and X.dtype == torch.bfloat16 and X.dim() == 2 and X.stride(1) == 1):
+        raise ValueError(f"{name} must be a 2-D bfloat16 CUDA tensor with contiguous rows")
+
+
+def gram(X, w=None, alpha: Optional[float] = None, beta: float = 0.0, out=None, stream=None):
+    """G = beta G + alpha X diag(w) X^T for samples X (d x N bf16, feature-major)
+    on the tensor cores (bakron_gram).  alpha defaults to 1/N (the sample
+    mean).  Returns (G float32 d x d, status int32[1])."""
+    torch = _torch()
+    lib = _lib.load()
+    _require_bf16_rows(X, "X")
+    d, N = X.shape
+    if w is not None:
+        _require_cuda_f32(w, (N,), "w")
+    G = torch.empty((d, d), dtype=torch.float32, device=X.device) if out is None else out
+    _require_cuda_f32(G, (d, d), "G")
+    status = torch.zeros(1, dtype=torch.int32, device=X.device)
+    a = 1.0 / N if alpha is None else float(alpha)
+    st = lib.bakron_gram(_ptr(X), d, N, X.stride(0), _ptr(w), a, float(beta), _ptr(G), _ptr(status),
+                         _stream_handle(stream))
+    _lib.check(st, "bakron_gram")
+    return G, status
+
+
+def sq_norms(Y, out=None, stream=None):
+    """|y_t|^2 of the columns of Y (m x N bf16): one Shampoo step's weights (bakron_sq_norms)."""
+    torch = _torch()
+    lib = _lib.load()
+    _require_bf16_rows(Y, "Y")
+    m, N = Y.shape
+    w = torch.empty(N, dtype=torch.float32, device=Y.device) if out is None else out
+    _require_cuda_f32(w, (N,), "w")
+    st = lib.bakron_sq_norms(_ptr(Y), m, N, Y.stride(0), _ptr(w), _stream_handle(stream))
+    _lib.check(st, "bakron_sq_norms")
+    return w
+
+
+def damp(G, rel: float = 0.5, stream=None):
+    """G += rel * mean(diag G) * I in place (bakron_damp; App. D: rel = 0.5)."""
+    lib = _lib.load()
+    d = G.shape[0]
+    _require_cuda_f32(G, (d, d), "G")
+    st = lib.bakron_damp(_ptr(G), d, float(rel), _stream_handle(stream))
+    _lib.check(st, "bakron_damp")
+    return G
 
 
 def quantize_range(W, LA, LB, scales, lo: int, hi: int, ws=None, out=None, stream=None):

@@ -171,6 +171,26 @@ int bakron_antidiag_quantize(const float* W, const float* LA, const float* LB, c
                                            Wq, ws, status_dev, (cudaStream_t)stream));
 }
 
+int bakron_gram(const void* X, int64_t d, int64_t N, int64_t ldx, const float* w, float alpha, float beta, float* G,
+                int32_t* status_dev, void* stream) {
+  if (!X || !G || !status_dev || d < 1 || N < 1 || ldx < N || ldx % 8 != 0) return BAKRON_ERR_INVALID_ARG;
+  if (d * d >= kMaxElems || d * ldx >= ((int64_t)1 << 40) || N >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || (w && !aligned(w, 16)) || (const void*)G == X) return BAKRON_ERR_INVALID_ARG;
+  return from_cuda(bakron::gram_launch(static_cast<const uint16_t*>(X), (int)d, (int)N, (int)ldx, w, alpha, beta, G,
+                                       status_dev, (cudaStream_t)stream));
+}
+
+int bakron_sq_norms(const void* Y, int64_t m, int64_t N, int64_t ldy, float* w, void* stream) {
+  if (!Y || !w || m < 1 || N < 1 || ldy < N || N >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  return from_cuda(bakron::sq_norms_launch(static_cast<const uint16_t*>(Y), (int)m, (int)N, (int)ldy, w,
+                                           (cudaStream_t)stream));
+}
+
+int bakron_damp(float* G, int64_t d, float rel, void* stream) {
+  if (!G || d < 1 || d * d >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
+  return from_cuda(bakron::damp_launch(G, (int)d, rel, (cudaStream_t)stream));
+}
+
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,

@@ -1,0 +1,298 @@
+// gram.cu -- Kronecker factors from calibration samples on the tensor cores
+// ("BaKron: Efficient Quantization with Kronecker-Factored Hessians",
+// Sec. 4.2 and App. A.2: K-FAC factors E[a a^T], E[b b^T]; one Shampoo step
+// E[|b|^2 a a^T], E[|a|^2 b b^T]; App. D: damping by 0.5 times the mean
+// diagonal):
+//     G <- beta G + alpha X diag(w) X^T
+// for samples X (d features x N samples, bfloat16, feature-major) and
+// optional per-sample weights w (fp32).
+//
+// Each CTA computes one 128 x 128 tile of the lower block triangle over all
+// N samples and writes it and its mirror.  Both operands are K-major rows of
+// X (K = samples): copies of 16 bytes land directly in the tcgen05 core-matrix
+// layout, one MMA of M = N = 128, K = 16 per 16 samples accumulates in
+// tensor memory (fp32; every bf16 x bf16 product is exact there).  With
+// weights, the column operand w_t x_t is split into two bf16 terms
+// (hi = bf16(w x), lo = bf16(w x - hi), about 2^-17 relative left over) and
+// multiplied in two MMAs.  Warp 0 issues the MMAs, warps 1..7 copy (three
+// stages in flight), warps 4..7 then read the accumulator out.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "bakron.h"
+#include "df.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace bakron {
+namespace {
+
+constexpr int kGT = 128;                 // output tile edge (tensor-memory lanes, MMA N)
+constexpr int kGK = 64;                  // samples per stage: 8 groups of 8 (16 bytes)
+constexpr int kGStages = 3;
+constexpr int kGWarps = 8;
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kGProducers = kGThreads - 32;  // warps 1..7
+constexpr uint32_t kGLbo = 128;           // stride of an 8-sample group within an 8-row block
+constexpr uint32_t kGSbo = 128 * (kGK / 8);  // stride of an 8-row block: 1024 bytes
+constexpr int kGTileBytes = kGT * kGK * 2;  // 16 KB
+constexpr int kGChunks = kGT * (kGK / 8);   // 16-byte chunks per tile: 1024
+
+template <bool kW>
+struct GramSmem {
+  alignas(128) unsigned char A[kGStages][kGTileBytes];
+  alignas(128) unsigned char B[kGStages][kW ? 2 : 1][kGTileBytes];
+  uint64_t full[kGStages];
+  uint64_t empty[kGStages];
+  uint64_t done;
+  uint32_t tmem_base;
+};
+
+struct GramParams {
+  const uint16_t* X;  // bf16 bit patterns, d x ldx
+  const float* w;
+  float* G;
+  int32_t* status;
+  int d, N, ldx;
+  float alpha, beta;
+};
+
+// Chunk c of a tile: 8-row block c / 64, sample group (c % 64) / 8, row
+// (within the block) c % 8, at byte (r/8) SBO + g LBO + (r%8) 16 = 16 c: a
+// warp's 32 chunks (8 rows x 4 groups) fill 512 contiguous bytes of shared
+// memory and read 64 contiguous bytes from each of 8 rows.
+__device__ __forceinline__ void gchunk(int c, int& r, int& g) {
+  r = 8 * (c / 64) + (c % 8);
+  g = (c % 64) / 8;
+}
+
+__device__ __forceinline__ void tri_index(int t, int& bi, int& bj) {
+  int i = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
+  while (i * (i + 1) / 2 > t) --i;
+  while ((i + 1) * (i + 2) / 2 <= t) ++i;
+  bi = i;
+  bj = t - i * (i + 1) / 2;
+}
+
+// Copies rows row0 .. row0+127 of X, samples k0 .. k0+63, into a tile (zeros
+// outside the matrix).
+__device__ __forceinline__ void gram_copy(const GramParams& P, unsigned char* tile, int row0, int k0, int ptid) {
+  for (int c = ptid; c < kGChunks; c += kGProducers) {
+    int r, g;
+    gchunk(c, r, g);
+    const int row = row0 + r, k = k0 + 8 * g;
+    const int nb = (row < P.d) ? 2 * max(0, min(8, P.N - k)) : 0;
+    const void* src = nb ? (const void*)(P.X + (size_t)row * P.ldx + k) : (const void*)P.X;
+    cp_async(tile + 16 * c, src, nb, 16);
+  }
+}
+
+// The weighted column operand: w_t x_t as hi + lo bf16 tiles.
+__device__ __forceinline__ void gram_weighted(const GramParams& P, unsigned char* hi, unsigned char* lo, int row0,
+                                              int k0, int ptid) {
+  for (int c = ptid; c < kGChunks; c += kGProducers) {
+    int r, g;
+    gchunk(c, r, g);
+    const int row = row0 + r;
+    {
+      const int k = k0 + 8 * g;
+      uint32_t xv[4] = {0u, 0u, 0u, 0u};
+      float wv[8];
+      if (row < P.d && k + 8 <= P.N) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(P.X + (size_t)row * P.ldx + k));
+        xv[0] = q.x, xv[1] = q.y, xv[2] = q.z, xv[3] = q.w;
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(P.w + k));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(P.w + k + 4));
+        wv[0] = w0.x, wv[1] = w0.y, wv[2] = w0.z, wv[3] = w0.w, wv[4] = w1.x, wv[5] = w1.y, wv[6] = w1.z, wv[7] = w1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool ok = row < P.d && k + e < P.N;
+          const uint32_t b = ok ? P.X[(size_t)row * P.ldx + k + e] : 0u;
+          xv[e / 2] |= b << (16 * (e % 2));
+          wv[e] = ok ? P.w[k + e] : 0.f;
+        }
+      }
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = __uint_as_float(xv[e] << 16), x1 = __uint_as_float(xv[e] & 0xFFFF0000u);
+        const float p0 = wv[2 * e] * x0, p1 = wv[2 * e + 1] * x1;
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(p0 - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+        hv[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lv[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      *reinterpret_cast<uint4*>(hi + 16 * c) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(lo + 16 * c) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+  }
+}
+
+template <bool kW>
+__global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
+  extern __shared__ __align__(1024) unsigned char g_smem_raw[];
+  GramSmem<kW>& sm = *reinterpret_cast<GramSmem<kW>*>(g_smem_raw);
+  int bi, bj;
+  tri_index(blockIdx.x, bi, bj);
+  const bool diag = bi == bj;
+  const bool copy_b = kW || !diag;  // the diagonal tile without weights multiplies A by itself
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nz = (P.N + kGK - 1) / kGK;
+  bool broken = false;
+
+  if (tid == 0) {
+    for (int i = 0; i < kGStages; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])), "r"(kGProducers));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.done)));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;\n" ::"r"(smem_u32(&sm.tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp > 0) {  // producers: stage z copied, then (S - 1 stages later) published
+    const int ptid = tid - 32;
+    for (int z = 0; z < nz + kGStages - 1; ++z) {
+      if (z < nz) {
+        const int slot = z % kGStages;
+        if (z >= kGStages) mbar_wait(&sm.empty[slot], (uint32_t)((z / kGStages) - 1) & 1u, broken);
+        gram_copy(P, sm.A[slot], bi * kGT, z * kGK, ptid);
+        if (kW) {
+          gram_weighted(P, sm.B[slot][0], sm.B[slot][kW ? 1 : 0], bj * kGT, z * kGK, ptid);
+        } else if (copy_b) {
+          gram_copy(P, sm.B[slot][0], bj * kGT, z * kGK, ptid);
+        }
+      }
+      cp_async_commit();
+      const int zr = z - (kGStages - 1);
+      if (zr >= 0) {
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(kGStages - 1) : "memory");
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[zr % kGStages])) : "memory");
+      }
+    }
+  } else if (lane == 0) {  // the MMA thread
+    constexpr uint32_t idesc = umma_idesc_bf16(kGT, kGT);
+    for (int z = 0; z < nz; ++z) {
+      const int slot = z % kGStages;
+      mbar_wait(&sm.full[slot], (uint32_t)(z / kGStages) & 1u, broken);
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sm.A[slot]);
+      const uint32_t b0 = copy_b ? smem_u32(sm.B[slot][0]) : a0;
+#pragma unroll
+      for (int j = 0; j < kGK / 16; ++j) {
+        const uint32_t off = (uint32_t)(2 * j) * kGLbo;
+        const uint64_t da = umma_sdesc(a0 + off, kGLbo, kGSbo);
+        umma_bf16(tmem, da, umma_sdesc(b0 + off, kGLbo, kGSbo), idesc, (z > 0 || j > 0) ? 1u : 0u);
+        if (kW) umma_bf16(tmem, da, umma_sdesc(smem_u32(sm.B[slot][kW ? 1 : 0]) + off, kGLbo, kGSbo), idesc, 1u);
+      }
+      umma_commit(&sm.empty[slot]);
+    }
+    umma_commit(&sm.done);
+  }
+  __syncwarp();
+
+  if (warp >= 4) {  // epilogue: tensor-memory lane quarter warp - 4, one output row per thread
+    const int q = warp - 4;
+    const int r = 32 * q + lane;
+    const int i = bi * kGT + r;
+    mbar_wait(&sm.done, 0u, broken);
+    tc_fence_after();
+    for (int c8 = 0; c8 < kGT / 8; ++c8) {
+      float v[8];
+      tmem_ld(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * c8), v);
+      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      // Entry (i, j) and its mirror (j, i); a diagonal tile writes its lower
+      // triangle and mirrors it, so G is exactly symmetric even where the
+      // two triangles' products were rounded differently (weighted split).
+      if (i < P.d && !broken) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = bj * kGT + 8 * c8 + e;
+          if (j >= P.d || (diag && j > i)) break;
+          float g = P.alpha * v[e];
+          if (P.beta != 0.f) g = fmaf(P.beta, P.G[(size_t)i * P.d + j], g);
+          P.G[(size_t)i * P.d + j] = g;
+          if (j != i) P.G[(size_t)j * P.d + i] = g;  // the mirror (coalesced across the warp)
+        }
+      }
+    }
+  }
+  if (broken) atomicOr(P.status, BAKRON_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;\n" ::"r"(tmem));
+}
+
+__global__ void sq_norms_kernel(const uint16_t* Y, int m, int N, int ldy, float* w) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= N) return;
+  float2 acc = make_float2(0.f, 0.f);  // double-float sum of exact squares
+  for (int i = 0; i < m; ++i) {
+    const float y = __uint_as_float((uint32_t)Y[(size_t)i * ldy + t] << 16);
+    acc = df_add(acc, two_prod(y, y));
+  }
+  w[t] = acc.x + acc.y;
+}
+
+// G + rel * mean(diag G) * I; one CTA of 1024 threads, the trace in double-float.
+__global__ void damp_kernel(float* G, int d, float rel) {
+  __shared__ float2 red[32];
+  float2 s = make_float2(0.f, 0.f);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) s = df_add(s, make_float2(G[(size_t)i * d + i], 0.f));
+  for (int o = 16; o; o >>= 1)
+    s = df_add(s, make_float2(__shfl_xor_sync(0xffffffffu, s.x, o), __shfl_xor_sync(0xffffffffu, s.y, o)));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  float2 tot = make_float2(0.f, 0.f);
+  for (int k = 0; k < (int)(blockDim.x >> 5); ++k) tot = df_add(tot, red[k]);
+  const float add = rel * __fdiv_rn(tot.x + tot.y, (float)d);
+  __syncthreads();
+  for (int i = threadIdx.x; i < d; i += blockDim.x) G[(size_t)i * d + i] += add;
+}
+
+}  // namespace
+
+cudaError_t gram_launch(const uint16_t* X, int d, int N, int ldx, const float* w, float alpha, float beta, float* G,
+                        int32_t* status_dev, cudaStream_t stream) {
+  GramParams P{X, w, G, status_dev, d, N, ldx, alpha, beta};
+  const int nb = (d + kGT - 1) / kGT;
+  const int tiles = nb * (nb + 1) / 2;
+  cudaError_t e = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
+  if (w) {
+    const size_t smem = sizeof(GramSmem<true>) + 1024;
+    e = cudaFuncSetAttribute(gram_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gram_kernel<true><<<tiles, kGThreads, smem, stream>>>(P);
+  } else {
+    const size_t smem = sizeof(GramSmem<false>) + 1024;
+    e = cudaFuncSetAttribute(gram_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gram_kernel<false><<<tiles, kGThreads, smem, stream>>>(P);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t sq_norms_launch(const uint16_t* Y, int m, int N, int ldy, float* w, cudaStream_t stream) {
+  sq_norms_kernel<<<(N + 255) / 256, 256, 0, stream>>>(Y, m, N, ldy, w);
+  return cudaGetLastError();
+}
+
+cudaError_t damp_launch(float* G, int d, float rel, cudaStream_t stream) {
+  damp_kernel<<<1, 1024, 0, stream>>>(G, d, rel);
+  return cudaGetLastError();
+}
+
+}  // namespace bakron

@@ -52,6 +52,12 @@ cudaError_t antidiag_launch(const float* W, const float* LA, const float* LB, co
                             int m, int n, int32_t* V, float* Wq, void* ws, int32_t* status_dev,
                             cudaStream_t stream);
 
+// gram.cu (Kronecker factors from samples)
+cudaError_t gram_launch(const uint16_t* X, int d, int N, int ldx, const float* w, float alpha, float beta, float* G,
+                        int32_t* status_dev, cudaStream_t stream);
+cudaError_t sq_norms_launch(const uint16_t* Y, int m, int N, int ldy, float* w, cudaStream_t stream);
+cudaError_t damp_launch(float* G, int d, float rel, cudaStream_t stream);
+
 // scales.cu
 // One scale per run of `group` columns of each row (group <= 0 or >= n: per
 // row), m x ceil(n / group) outputs.

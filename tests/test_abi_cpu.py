@@ -168,3 +168,21 @@ def test_antidiag_entry_point_rejects_bad_arguments(lib):
     assert a(W, W, W, None, 4, 8, 8, V, V, ws, need, W, None) == 1  # V aliases Wq
     assert a(W, W, W, None, 4, 8, 8, V, Wq, ws, need - 1, W, None) == 4  # small workspace
     assert a(W, W, W, None, 4, 8, 8, V, Wq, ctypes.c_void_p(0x100010), need, W, None) == 4  # misaligned
+
+
+def test_gram_entry_points_reject_bad_arguments(lib):
+    X, G, st = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    w = ctypes.c_void_p(0x4000)
+    g = lib.bakron_gram
+    assert g(X, 0, 8, 8, None, 1.0, 0.0, G, st, None) == 1  # d < 1
+    assert g(X, 8, 0, 8, None, 1.0, 0.0, G, st, None) == 1  # N < 1
+    assert g(X, 8, 9, 8, None, 1.0, 0.0, G, st, None) == 1  # ldx < N
+    assert g(X, 8, 6, 6, None, 1.0, 0.0, G, st, None) == 1  # ldx not a multiple of 8
+    assert g(ctypes.c_void_p(0x1008), 8, 8, 8, None, 1.0, 0.0, G, st, None) == 1  # X not 16-byte aligned
+    assert g(X, 8, 8, 8, ctypes.c_void_p(0x4004), 1.0, 0.0, G, st, None) == 1  # w not 16-byte aligned
+    assert g(X, 8, 8, 8, w, 1.0, 0.0, X, st, None) == 1  # G aliases X
+    assert g(X, 8, 8, 8, w, 1.0, 0.0, G, None, None) == 1  # no status word
+    assert lib.bakron_sq_norms(X, 4, 8, 7, w, None) == 1  # ldy < N
+    assert lib.bakron_sq_norms(None, 4, 8, 8, w, None) == 1
+    assert lib.bakron_damp(None, 4, 0.5, None) == 1
+    assert lib.bakron_damp(G, 0, 0.5, None) == 1
