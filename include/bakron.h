@@ -310,6 +310,15 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
                          int bits, int64_t m, int64_t n, int32_t* V, float* Wq, void* dev_ws,
                          size_t dev_ws_bytes, int32_t* status_host, void* stream);
 
+/* --------------------------------------------------------------- self-test
+ * Exercises the device-side timeout path on purpose: one thread waits, with
+ * the bounded wait the tensor-core kernels use (about 0.1 s, 2^28 cycles),
+ * on an mbarrier that nothing ever arrives on, gives up and sets
+ * *status_dev = BAKRON_DEV_TIMEOUT.  Nothing faults or hangs, and the
+ * context stays usable.  status_dev: device int32.  Enqueued on `stream`.
+ */
+int bakron_selftest_wait_timeout(int32_t* status_dev, void* stream);
+
 /* ------------------------------------------------------- no-allocation solve
  * For callers that cannot allocate device memory at all: a plugin inside a
  * host application whose device memory is entirely owned by another

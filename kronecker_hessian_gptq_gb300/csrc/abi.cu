@@ -191,6 +191,11 @@ int bakron_damp(float* G, int64_t d, float rel, void* stream) {
   return from_cuda(bakron::damp_launch(G, (int)d, rel, (cudaStream_t)stream));
 }
 
+int bakron_selftest_wait_timeout(int32_t* status_dev, void* stream) {
+  if (!status_dev) return BAKRON_ERR_INVALID_ARG;
+  return from_cuda(bakron::wait_selftest_launch(status_dev, (cudaStream_t)stream));
+}
+
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,

@@ -17,9 +17,9 @@
 // launch k + 1.  An output tile of 32 x 32 stages M[p, i] = L_B[p, i] Delta_i
 // (double-float) and L_A[q, k - i] for 32 diagonal entries at a time in
 // shared memory, the next chunk's operands loaded into registers while the
-// current one is multiplied; each thread accumulates a 2 x 4 block with
-// offset accumulators (5 fp32 instructions per multiply-add, two 16-byte
-// shared loads per 8 of them).  Small tiles keep the longest tile short:
+// current one is multiplied; each thread accumulates a 2 x 4 block (2 x 2
+// on layers of up to 2^21 weights) with offset accumulators (5 fp32
+// instructions per multiply-add).  Small tiles keep the longest tile short:
 // within one launch the tile nearest the end has the most terms, up to the
 // anti-diagonal's length.
 #include <algorithm>
@@ -32,11 +32,17 @@ namespace bakron {
 namespace {
 
 constexpr int kAdT = 32;         // output tile edge
-constexpr int kAdRM = 2;         // rows per thread
-constexpr int kAdRN = 4;         // columns per thread
-constexpr int kAdThreads = (kAdT / kAdRM) * (kAdT / kAdRN);  // 128
 constexpr int kAdKC = 32;        // diagonal entries per shared-memory stage
-constexpr int kAdSlots = kAdKC * kAdT / kAdThreads;  // staging slots per thread
+constexpr int kAdRM = 2;         // rows per thread
+// Columns per thread RN: 4 (128 threads, two 16-byte shared loads per 8
+// multiply-adds) for large layers, where throughput counts; 2 (256 threads,
+// half the work per thread) for small ones, where the tile with the most
+// terms sets the time of each launch.
+template <int RN>
+struct AdShape {
+  static constexpr int kThreads = (kAdT / kAdRM) * (kAdT / RN);
+  static constexpr int kSlots = kAdKC * kAdT / kThreads;  // staging slots per thread
+};
 constexpr int kAdPadM = kAdT + 2;  // row strides: 16-byte rows for vector loads
 constexpr int kAdPadL = kAdT + 4;
 
@@ -94,15 +100,18 @@ __device__ __forceinline__ void ad_round(const AdParams& P, int p, int q, float2
 // columns r): L_B[p, i] (1 on the diagonal, 0 where p < i or outside),
 // L_A[q, k - i] (likewise), and Delta_i -- one kk per thread, so one Delta.
 // Loaded a chunk ahead into registers.
-static_assert(kAdThreads % kAdKC == 0, "a thread's slots share one diagonal entry");
+template <int RN>
 struct AdSlot {
-  float l[kAdSlots];
-  float a[kAdSlots];
+  static_assert(AdShape<RN>::kThreads % kAdKC == 0, "a thread's slots share one diagonal entry");
+  float l[AdShape<RN>::kSlots];
+  float a[AdShape<RN>::kSlots];
   float2 d;
 };
 
+template <int RN>
 __device__ __forceinline__ void ad_load(const AdParams& P, const float2* D, int k, int ib, int i1, int P0, int Q0,
-                                        AdSlot& st) {
+                                        AdSlot<RN>& st) {
+  constexpr int kAdThreads = AdShape<RN>::kThreads, kAdSlots = AdShape<RN>::kSlots;
   const int kk = threadIdx.x % kAdKC;
   const int i = ib + kk, j = k - i;
   const bool vi = i <= i1;
@@ -118,7 +127,10 @@ __device__ __forceinline__ void ad_load(const AdParams& P, const float2* D, int 
 
 // Launch k (k = -1 .. m + n - 3): the update from anti-diagonal k (none for
 // k = -1), then the rounding of anti-diagonal k + 1.
-__global__ void __launch_bounds__(kAdThreads, 4) ad_step_kernel(AdParams P, int k) {
+template <int RN>
+__global__ void __launch_bounds__(AdShape<RN>::kThreads, 512 / AdShape<RN>::kThreads) ad_step_kernel(AdParams P,
+                                                                                                      int k) {
+  constexpr int kAdRN = RN, kAdThreads = AdShape<RN>::kThreads, kAdSlots = AdShape<RN>::kSlots;
   const int P0 = blockIdx.y * kAdT, Q0 = blockIdx.x * kAdT;
   const int pmax = min(P0 + kAdT, P.m) - 1, qmax = min(Q0 + kAdT, P.n) - 1;
   if (pmax + qmax <= k) return;  // every entry of the tile is rounded
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(kAdThreads, 4) ad_step_kernel(AdParams P, int 
   __shared__ __align__(16) float2 sM[kAdKC][kAdPadM];  // L_B[p, i] Delta_i
   __shared__ __align__(16) float sL[kAdKC][kAdPadL];   // L_A[q, k - i]
   __shared__ float sMax[2][kAdThreads / 32];           // per-warp max |M|, max |L_A| of the chunk
-  const int tr = threadIdx.x / (kAdT / kAdRN), tc = threadIdx.x % (kAdT / kAdRN);  // rows 2 tr.., columns 4 tc..
+  const int tr = threadIdx.x / (kAdT / kAdRN), tc = threadIdx.x % (kAdT / kAdRN);  // rows 2 tr.., columns RN tc..
   // Each chunk of at most kAdKC terms is summed by offset accumulators on an
   // offset of its own, from the chunk's largest operands, and folded into a
   // double-float total: the rounding error then scales with the terms
@@ -145,7 +157,7 @@ __global__ void __launch_bounds__(kAdThreads, 4) ad_step_kernel(AdParams P, int 
 #pragma unroll
     for (int b = 0; b < kAdRN; ++b) tot[a][b] = make_float2(0.f, 0.f);
 
-  AdSlot st;
+  AdSlot<RN> st;
   if (i0 <= i1) ad_load(P, D, k, i0, i1, P0, Q0, st);
   for (int ib = i0; ib <= i1; ib += kAdKC) {
     float mmax = 0.f, lmax = 0.f;
@@ -186,16 +198,20 @@ __global__ void __launch_bounds__(kAdThreads, 4) ad_step_kernel(AdParams P, int 
 #pragma unroll 4
     for (int kk = 0; kk < kn; ++kk) {
       const float4 mm = *reinterpret_cast<const float4*>(&sM[kk][kAdRM * tr]);  // rows 2 tr, 2 tr + 1
-      const float4 ll = *reinterpret_cast<const float4*>(&sL[kk][kAdRN * tc]);  // columns 4 tc .. 4 tc + 3
       const float2 m0 = make_float2(mm.x, mm.y), m1 = make_float2(mm.z, mm.w);
-      acc[0][0].mac(ll.x, m0);
-      acc[0][1].mac(ll.y, m0);
-      acc[0][2].mac(ll.z, m0);
-      acc[0][3].mac(ll.w, m0);
-      acc[1][0].mac(ll.x, m1);
-      acc[1][1].mac(ll.y, m1);
-      acc[1][2].mac(ll.z, m1);
-      acc[1][3].mac(ll.w, m1);
+      float lv[kAdRN];
+      if constexpr (kAdRN == 4) {
+        const float4 ll = *reinterpret_cast<const float4*>(&sL[kk][4 * tc]);  // columns 4 tc .. 4 tc + 3
+        lv[0] = ll.x, lv[1] = ll.y, lv[2] = ll.z, lv[3] = ll.w;
+      } else {
+        const float2 ll = *reinterpret_cast<const float2*>(&sL[kk][2 * tc]);  // columns 2 tc, 2 tc + 1
+        lv[0] = ll.x, lv[1] = ll.y;
+      }
+#pragma unroll
+      for (int b = 0; b < kAdRN; ++b) {
+        acc[0][b].mac(lv[b], m0);
+        acc[1][b].mac(lv[b], m1);
+      }
     }
 #pragma unroll
     for (int a = 0; a < kAdRM; ++a)
@@ -263,7 +279,11 @@ cudaError_t antidiag_launch(const float* W, const float* LA, const float* LB, co
   const int pre_blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
   ad_prepass_kernel<<<pre_blocks, 256, 0, stream>>>(P);
   const dim3 grid((unsigned)((n + kAdT - 1) / kAdT), (unsigned)((m + kAdT - 1) / kAdT));
-  for (int k = -1; k <= m + n - 3; ++k) ad_step_kernel<<<grid, kAdThreads, 0, stream>>>(P, k);
+  if ((int64_t)m * n <= (int64_t)1 << 21) {
+    for (int k = -1; k <= m + n - 3; ++k) ad_step_kernel<2><<<grid, AdShape<2>::kThreads, 0, stream>>>(P, k);
+  } else {
+    for (int k = -1; k <= m + n - 3; ++k) ad_step_kernel<4><<<grid, AdShape<4>::kThreads, 0, stream>>>(P, k);
+  }
   return cudaGetLastError();
 }
 

@@ -58,6 +58,9 @@ cudaError_t gram_launch(const uint16_t* X, int d, int N, int ldx, const float* w
 cudaError_t sq_norms_launch(const uint16_t* Y, int m, int N, int ldy, float* w, cudaStream_t stream);
 cudaError_t damp_launch(float* G, int d, float rel, cudaStream_t stream);
 
+// selftest.cu
+cudaError_t wait_selftest_launch(int32_t* status_dev, cudaStream_t stream);
+
 // scales.cu
 // One scale per run of `group` columns of each row (group <= 0 or >= n: per
 // row), m x ceil(n / group) outputs.

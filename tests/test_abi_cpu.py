@@ -186,3 +186,7 @@ def test_gram_entry_points_reject_bad_arguments(lib):
     assert lib.bakron_sq_norms(None, 4, 8, 8, w, None) == 1
     assert lib.bakron_damp(None, 4, 0.5, None) == 1
     assert lib.bakron_damp(G, 0, 0.5, None) == 1
+
+
+def test_selftest_rejects_a_missing_status_word(lib):
+    assert lib.bakron_selftest_wait_timeout(None, None) == 1

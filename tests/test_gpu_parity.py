@@ -170,3 +170,23 @@ def test_host_entry_point_matches_device_entry_point(bk):
                                    torch.from_numpy(p.scales), p.bits)
     assert st == 0
     assert np.array_equal(Vh.numpy(), Vd) and np.array_equal(Wqh.numpy(), Wqd)
+
+
+def test_bounded_wait_reports_a_timeout_and_the_context_survives(bk):
+    """The tensor-core kernels' bounded mbarrier wait, run on a barrier that
+    nothing arrives on: the device status reads BAKRON_DEV_TIMEOUT, and a
+    solve afterwards still runs and matches the oracle."""
+    import torch
+
+    from kronecker_hessian_gptq_gb300 import _lib
+
+    lib = bk.load_library()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _lib.check(lib.bakron_selftest_wait_timeout(status.data_ptr(), torch.cuda.current_stream().cuda_stream),
+               "bakron_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    assert int(status.item()) == 4  # BAKRON_DEV_TIMEOUT
+    p = random_problem(40, 50, bits=4, seed=8)
+    LA, LB = gpu_prepare(bk, p)
+    V, Wq = gpu_quantize(bk, p, LA, LB)
+    check_against_oracle(p, V, Wq, *O.factors_of(p.A, p.B), "after timeout")
