@@ -379,7 +379,7 @@ def run_gram(args, world, dev):
         "config": {"workload": f"{s.name}: {d} features x {N} samples, Student-t (nu = 4)", "d": d, "N": N,
                    "l2": f"inputs ({d * N * 2 / 2**20:.0f} MiB) larger than L2"},
         "shampoo_ms": shampoo_ms, "shampoo_tflops": flops / (shampoo_ms * 1e-3) / 1e12,
-        "clocks": clocks, "gpu_launches": 2 * (args.warmup + args.steps),
+        "clocks": clocks, "gpu_launches": 2 * args.steps,  # per K-FAC call: the packing pass and the products
         "roofline": {"bound": "tensor", "kernel": "gram_kernel", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                      "peak_basis": ("measured" if "bf16_tflops" in peaks else "fallback")

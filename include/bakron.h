@@ -164,8 +164,14 @@ int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, i
  * samples is accumulated with beta = 1 and alpha = 1 / (total samples).
  */
 
+/* Workspace bytes of bakron_gram: the samples repacked into 16 KB blocks
+ * (128 features x 64 samples, zero-padded), three copies with weights. */
+size_t bakron_gram_workspace_size(int64_t d, int64_t N, int weighted);
+
 /* G <- beta G + alpha X diag(w) X^T on the tensor cores (tcgen05; every
- * bf16 product exact, fp32 accumulation over the samples).
+ * bf16 product exact, fp32 accumulation over the samples).  A packing pass
+ * rearranges X into `ws` first; the products then stream 16 KB blocks with
+ * bulk copies.
  * X: device, bf16 bit patterns, d x ldx, 16-byte aligned, ldx >= N and a
  *    multiple of 8.
  * w: device, N fp32 per-sample weights, 16-byte aligned, or NULL for ones.
@@ -173,12 +179,14 @@ int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, i
  *    relative remains) and multiplied in two products.
  * G: device, d x d fp32, written in full (both triangles, symmetric); with
  *    beta != 0 it must be symmetric on entry.  Not aliasing X.
+ * ws: device, >= bakron_gram_workspace_size(d, N, w != NULL) bytes, 256-byte
+ *    aligned; its contents on entry do not matter.
  * status_dev: device int32, set to 0 or BAKRON_DEV_TIMEOUT.
  * d, N >= 1, d * d < 2^31.  One CTA per 128 x 128 tile of the lower block
  * triangle, enqueued on `stream`.
  */
 int bakron_gram(const void* X, int64_t d, int64_t N, int64_t ldx, const float* w, float alpha, float beta, float* G,
-                int32_t* status_dev, void* stream);
+                void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /* w[t] = |y_t|^2 for the columns of Y (device, bf16, m x ldy, ldy >= N): the
  * weights of one Shampoo step (squares exact, sums in double-float). */

@@ -197,7 +197,7 @@ def _require_bf16_rows(X, name):
         raise ValueError(f"{name} must be a 2-D bfloat16 CUDA tensor with contiguous rows")
 
 
-def gram(X, w=None, alpha: Optional[float] = None, beta: float = 0.0, out=None, stream=None):
+def gram(X, w=None, alpha: Optional[float] = None, beta: float = 0.0, out=None, ws=None, stream=None):
     """G = beta G + alpha X diag(w) X^T for samples X (d x N bf16, feature-major)
     on the tensor cores (bakron_gram).  alpha defaults to 1/N (the sample
     mean).  Returns (G float32 d x d, status int32[1])."""
@@ -211,8 +211,10 @@ def gram(X, w=None, alpha: Optional[float] = None, beta: float = 0.0, out=None, 
     _require_cuda_f32(G, (d, d), "G")
     status = torch.zeros(1, dtype=torch.int32, device=X.device)
     a = 1.0 / N if alpha is None else float(alpha)
-    st = lib.bakron_gram(_ptr(X), d, N, X.stride(0), _ptr(w), a, float(beta), _ptr(G), _ptr(status),
-                         _stream_handle(stream))
+    if ws is None:
+        ws = _workspace(lib.bakron_gram_workspace_size(d, N, int(w is not None)), X.device)
+    st = lib.bakron_gram(_ptr(X), d, N, X.stride(0), _ptr(w), a, float(beta), _ptr(G), _ptr(ws), ws.numel(),
+                         _ptr(status), _stream_handle(stream))
     _lib.check(st, "bakron_gram")
     return G, status
 

@@ -49,7 +49,8 @@ SIGNATURES = {
     "bakron_pack_codes": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
     "bakron_antidiag_workspace_size": (_sz, [_i64, _i64]),
     "bakron_antidiag_quantize": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
-    "bakron_gram": (_int, [_vp, _i64, _i64, _i64, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]),
+    "bakron_gram_workspace_size": (_sz, [_i64, _i64, _int]),
+    "bakron_gram": (_int, [_vp, _i64, _i64, _i64, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp, _sz, _vp, _vp]),
     "bakron_sq_norms": (_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
     "bakron_damp": (_int, [_vp, _i64, ctypes.c_float, _vp]),
     "bakron_selftest_wait_timeout": (_int, [_vp, _vp]),

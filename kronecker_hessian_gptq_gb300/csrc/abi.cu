@@ -171,13 +171,20 @@ int bakron_antidiag_quantize(const float* W, const float* LA, const float* LB, c
                                            Wq, ws, status_dev, (cudaStream_t)stream));
 }
 
+size_t bakron_gram_workspace_size(int64_t d, int64_t N, int weighted) {
+  if (d < 1 || N < 1 || d * d >= kMaxElems || N >= kMaxElems) return 0;
+  return bakron::gram_workspace_bytes(d, N, weighted != 0);
+}
+
 int bakron_gram(const void* X, int64_t d, int64_t N, int64_t ldx, const float* w, float alpha, float beta, float* G,
-                int32_t* status_dev, void* stream) {
+                void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
   if (!X || !G || !status_dev || d < 1 || N < 1 || ldx < N || ldx % 8 != 0) return BAKRON_ERR_INVALID_ARG;
   if (d * d >= kMaxElems || d * ldx >= ((int64_t)1 << 40) || N >= kMaxElems) return BAKRON_ERR_INVALID_ARG;
   if (!aligned(X, 16) || (w && !aligned(w, 16)) || (const void*)G == X) return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::gram_workspace_bytes(d, N, w != nullptr))
+    return BAKRON_ERR_WORKSPACE;
   return from_cuda(bakron::gram_launch(static_cast<const uint16_t*>(X), (int)d, (int)N, (int)ldx, w, alpha, beta, G,
-                                       status_dev, (cudaStream_t)stream));
+                                       ws, status_dev, (cudaStream_t)stream));
 }
 
 int bakron_sq_norms(const void* Y, int64_t m, int64_t N, int64_t ldy, float* w, void* stream) {

@@ -7,15 +7,17 @@
 // for samples X (d features x N samples, bfloat16, feature-major) and
 // optional per-sample weights w (fp32).
 //
-// Each CTA computes one 128 x 128 tile of the lower block triangle over all
-// N samples and writes it and its mirror.  Both operands are K-major rows of
-// X (K = samples): copies of 16 bytes land directly in the tcgen05 core-matrix
-// layout, one MMA of M = N = 128, K = 16 per 16 samples accumulates in
-// tensor memory (fp32; every bf16 x bf16 product is exact there).  With
-// weights, the column operand w_t x_t is split into two bf16 terms
-// (hi = bf16(w x), lo = bf16(w x - hi), about 2^-17 relative left over) and
-// multiplied in two MMAs.  Warp 0 issues the MMAs, warps 1..7 copy (three
-// stages in flight), warps 4..7 then read the accumulator out.
+// A packing pass first rearranges X into 16 KB blocks of 128 rows x 64
+// samples, each already in the tcgen05 core-matrix layout (K = samples), in
+// one streaming read and write.  With weights it also writes the column
+// operand w_t x_t split into two bf16 terms (hi = bf16(w x), lo = bf16(w x -
+// hi), about 2^-17 relative left over), multiplied in two MMAs.  Each CTA of
+// the Gram kernel then computes one 128 x 128 tile of the lower block
+// triangle over all N samples: one thread loads each stage with two (three)
+// 1-D bulk copies of 16 KB that complete on the stage's mbarrier, one
+// thread issues an MMA of M = N = 128, K = 16 per 16 samples into tensor
+// memory (fp32; every bf16 x bf16 product is exact there), and four warps
+// read the tile out and write it and its mirror.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -33,11 +35,10 @@ constexpr int kGK = 64;                  // samples per stage: 8 groups of 8 (16
 constexpr int kGStages = 3;
 constexpr int kGWarps = 8;
 constexpr int kGThreads = kGWarps * 32;
-constexpr int kGProducers = kGThreads - 32;  // warps 1..7
-constexpr uint32_t kGLbo = 128;           // stride of an 8-sample group within an 8-row block
+constexpr uint32_t kGLbo = 128;              // stride of an 8-sample group within an 8-row block
 constexpr uint32_t kGSbo = 128 * (kGK / 8);  // stride of an 8-row block: 1024 bytes
-constexpr int kGTileBytes = kGT * kGK * 2;  // 16 KB
-constexpr int kGChunks = kGT * (kGK / 8);   // 16-byte chunks per tile: 1024
+constexpr int kGTileBytes = kGT * kGK * 2;   // 16 KB
+constexpr int kGChunks = kGT * (kGK / 8);    // 16-byte chunks per block: 1024
 
 template <bool kW>
 struct GramSmem {
@@ -49,19 +50,21 @@ struct GramSmem {
   uint32_t tmem_base;
 };
 
+// Packed samples: block (rb, kb) holds rows 128 rb .. +127 and samples
+// 64 kb .. +63 as 16 KB in the tcgen05 core-matrix layout (K-major, no
+// swizzle): chunk c (16 bytes, 8 samples) is row 8 (c / 64) + c % 8, sample
+// group (c % 64) / 8, so that byte 16 c = (r/8) SBO + g LBO + (r%8) 16.
+// Blocks are stored block-row-major, [rb][kb].
 struct GramParams {
-  const uint16_t* X;  // bf16 bit patterns, d x ldx
-  const float* w;
+  const unsigned char* Xa;   // packed samples (row operand)
+  const unsigned char* Xb;   // packed column operand: the samples, or w x's high part
+  const unsigned char* Xl;   // low part of w x (weighted only)
   float* G;
   int32_t* status;
-  int d, N, ldx;
+  int d, nkb;
   float alpha, beta;
 };
 
-// Chunk c of a tile: 8-row block c / 64, sample group (c % 64) / 8, row
-// (within the block) c % 8, at byte (r/8) SBO + g LBO + (r%8) 16 = 16 c: a
-// warp's 32 chunks (8 rows x 4 groups) fill 512 contiguous bytes of shared
-// memory and read 64 contiguous bytes from each of 8 rows.
 __device__ __forceinline__ void gchunk(int c, int& r, int& g) {
   r = 8 * (c / 64) + (c % 8);
   g = (c % 64) / 8;
@@ -75,60 +78,53 @@ __device__ __forceinline__ void tri_index(int t, int& bi, int& bj) {
   bj = t - i * (i + 1) / 2;
 }
 
-// Copies rows row0 .. row0+127 of X, samples k0 .. k0+63, into a tile (zeros
-// outside the matrix).
-__device__ __forceinline__ void gram_copy(const GramParams& P, unsigned char* tile, int row0, int k0, int ptid) {
-  for (int c = ptid; c < kGChunks; c += kGProducers) {
+// One thread per 16-byte chunk of the packed arrays: the samples (zeros
+// outside the matrix) and, with weights, w_t x_t split into bf16 hi + lo.
+__global__ void gram_pack_kernel(const uint16_t* X, int d, int N, int ldx, const float* w, int nkb,
+                                 unsigned char* Xa, unsigned char* Xh, unsigned char* Xl) {
+  const size_t total = (size_t)((d + kGT - 1) / kGT) * nkb * kGChunks;
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const size_t blk = idx / kGChunks;
+    const int c = (int)(idx % kGChunks);
+    const int rb = (int)(blk / nkb), kb = (int)(blk % nkb);
     int r, g;
     gchunk(c, r, g);
-    const int row = row0 + r, k = k0 + 8 * g;
-    const int nb = (row < P.d) ? 2 * max(0, min(8, P.N - k)) : 0;
-    const void* src = nb ? (const void*)(P.X + (size_t)row * P.ldx + k) : (const void*)P.X;
-    cp_async(tile + 16 * c, src, nb, 16);
-  }
-}
-
-// The weighted column operand: w_t x_t as hi + lo bf16 tiles.
-__device__ __forceinline__ void gram_weighted(const GramParams& P, unsigned char* hi, unsigned char* lo, int row0,
-                                              int k0, int ptid) {
-  for (int c = ptid; c < kGChunks; c += kGProducers) {
-    int r, g;
-    gchunk(c, r, g);
-    const int row = row0 + r;
-    {
-      const int k = k0 + 8 * g;
-      uint32_t xv[4] = {0u, 0u, 0u, 0u};
-      float wv[8];
-      if (row < P.d && k + 8 <= P.N) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(P.X + (size_t)row * P.ldx + k));
-        xv[0] = q.x, xv[1] = q.y, xv[2] = q.z, xv[3] = q.w;
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(P.w + k));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(P.w + k + 4));
-        wv[0] = w0.x, wv[1] = w0.y, wv[2] = w0.z, wv[3] = w0.w, wv[4] = w1.x, wv[5] = w1.y, wv[6] = w1.z, wv[7] = w1.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool ok = row < P.d && k + e < P.N;
-          const uint32_t b = ok ? P.X[(size_t)row * P.ldx + k + e] : 0u;
-          xv[e / 2] |= b << (16 * (e % 2));
-          wv[e] = ok ? P.w[k + e] : 0.f;
-        }
-      }
+    const int row = rb * kGT + r, k = kb * kGK + 8 * g;
+    uint32_t xv[4] = {0u, 0u, 0u, 0u};
+    if (row < d && k + 8 <= N) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(X + (size_t)row * ldx + k));
+      xv[0] = q.x, xv[1] = q.y, xv[2] = q.z, xv[3] = q.w;
+    } else if (row < d) {
+      for (int e = 0; e < 8 && k + e < N; ++e) xv[e / 2] |= (uint32_t)X[(size_t)row * ldx + k + e] << (16 * (e % 2));
+    }
+    reinterpret_cast<uint4*>(Xa)[idx] = make_uint4(xv[0], xv[1], xv[2], xv[3]);
+    if (w) {
       uint32_t hv[4], lv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float x0 = __uint_as_float(xv[e] << 16), x1 = __uint_as_float(xv[e] & 0xFFFF0000u);
-        const float p0 = wv[2 * e] * x0, p1 = wv[2 * e + 1] * x1;
+        const int k0 = k + 2 * e;
+        const float w0 = (row < d && k0 < N) ? w[k0] : 0.f, w1 = (row < d && k0 + 1 < N) ? w[k0 + 1] : 0.f;
+        const float p0 = w0 * __uint_as_float(xv[e] << 16), p1 = w1 * __uint_as_float(xv[e] & 0xFFFF0000u);
         const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
         const __nv_bfloat16 l0 = __float2bfloat16_rn(p0 - __bfloat162float(h0));
         const __nv_bfloat16 l1 = __float2bfloat16_rn(p1 - __bfloat162float(h1));
         hv[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
         lv[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
       }
-      *reinterpret_cast<uint4*>(hi + 16 * c) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      *reinterpret_cast<uint4*>(lo + 16 * c) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      reinterpret_cast<uint4*>(Xh)[idx] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      reinterpret_cast<uint4*>(Xl)[idx] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
   }
+}
+
+// A 1-D bulk copy global -> shared (the TMA engine, no tensor map), counted
+// on the mbarrier's transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+               : "memory");
 }
 
 template <bool kW>
@@ -140,12 +136,12 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   const bool diag = bi == bj;
   const bool copy_b = kW || !diag;  // the diagonal tile without weights multiplies A by itself
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nz = (P.N + kGK - 1) / kGK;
+  const int nz = P.nkb;
   bool broken = false;
 
   if (tid == 0) {
     for (int i = 0; i < kGStages; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])), "r"(kGProducers));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.full[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.done)));
@@ -160,32 +156,26 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp > 0) {  // producers: stage z copied, then (S - 1 stages later) published
-    const int ptid = tid - 32;
-    for (int z = 0; z < nz + kGStages - 1; ++z) {
-      if (z < nz) {
-        const int slot = z % kGStages;
-        if (z >= kGStages) mbar_wait(&sm.empty[slot], (uint32_t)((z / kGStages) - 1) & 1u, broken);
-        gram_copy(P, sm.A[slot], bi * kGT, z * kGK, ptid);
-        if (kW) {
-          gram_weighted(P, sm.B[slot][0], sm.B[slot][kW ? 1 : 0], bj * kGT, z * kGK, ptid);
-        } else if (copy_b) {
-          gram_copy(P, sm.B[slot][0], bj * kGT, z * kGK, ptid);
-        }
-      }
-      cp_async_commit();
-      const int zr = z - (kGStages - 1);
-      if (zr >= 0) {
-        asm volatile("cp.async.wait_group %0;\n" ::"n"(kGStages - 1) : "memory");
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[zr % kGStages])) : "memory");
-      }
+  if (warp == 1 && lane == 0) {  // the copy thread: each stage is two (three) bulk copies of 16 KB
+    const uint32_t bytes = (uint32_t)kGTileBytes * (1u + (copy_b ? 1u : 0u) + (kW ? 1u : 0u));
+    const size_t rowa = (size_t)bi * P.nkb, rowb = (size_t)bj * P.nkb;
+    for (int z = 0; z < nz; ++z) {
+      const int slot = z % kGStages;
+      if (z >= kGStages) mbar_wait(&sm.empty[slot], (uint32_t)((z / kGStages) - 1) & 1u, broken);
+      if (broken) break;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[slot])),
+                   "r"(bytes)
+                   : "memory");
+      bulk_g2s(sm.A[slot], P.Xa + (rowa + z) * kGTileBytes, kGTileBytes, &sm.full[slot]);
+      if (copy_b) bulk_g2s(sm.B[slot][0], P.Xb + (rowb + z) * kGTileBytes, kGTileBytes, &sm.full[slot]);
+      if (kW) bulk_g2s(sm.B[slot][kW ? 1 : 0], P.Xl + (rowb + z) * kGTileBytes, kGTileBytes, &sm.full[slot]);
     }
-  } else if (lane == 0) {  // the MMA thread
+  } else if (warp == 0 && lane == 0) {  // the MMA thread
     constexpr uint32_t idesc = umma_idesc_bf16(kGT, kGT);
     for (int z = 0; z < nz; ++z) {
       const int slot = z % kGStages;
       mbar_wait(&sm.full[slot], (uint32_t)(z / kGStages) & 1u, broken);
+      if (broken) break;
       tc_fence_after();
       const uint32_t a0 = smem_u32(sm.A[slot]);
       const uint32_t b0 = copy_b ? smem_u32(sm.B[slot][0]) : a0;
@@ -264,13 +254,26 @@ __global__ void damp_kernel(float* G, int d, float rel) {
 
 }  // namespace
 
+size_t gram_workspace_bytes(int64_t d, int64_t N, bool weighted) {
+  const size_t blocks = (size_t)((d + kGT - 1) / kGT) * (size_t)((N + kGK - 1) / kGK);
+  return blocks * kGTileBytes * (weighted ? 3 : 1);
+}
+
 cudaError_t gram_launch(const uint16_t* X, int d, int N, int ldx, const float* w, float alpha, float beta, float* G,
-                        int32_t* status_dev, cudaStream_t stream) {
-  GramParams P{X, w, G, status_dev, d, N, ldx, alpha, beta};
+                        void* ws, int32_t* status_dev, cudaStream_t stream) {
   const int nb = (d + kGT - 1) / kGT;
+  const int nkb = (N + kGK - 1) / kGK;
+  const size_t plane = (size_t)nb * nkb * kGTileBytes;
+  unsigned char* Xa = static_cast<unsigned char*>(ws);
+  unsigned char* Xh = w ? Xa + plane : nullptr;
+  unsigned char* Xl = w ? Xa + 2 * plane : nullptr;
+  GramParams P{Xa, w ? Xh : Xa, Xl, G, status_dev, d, nkb, alpha, beta};
   const int tiles = nb * (nb + 1) / 2;
   cudaError_t e = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
+  const size_t chunks = plane / 16;
+  const int pack_blocks = (int)std::min<size_t>((chunks + 255) / 256, 152 * 16);
+  gram_pack_kernel<<<pack_blocks, 256, 0, stream>>>(X, d, N, ldx, w, nkb, Xa, Xh, Xl);
   if (w) {
     const size_t smem = sizeof(GramSmem<true>) + 1024;
     e = cudaFuncSetAttribute(gram_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -53,8 +53,9 @@ cudaError_t antidiag_launch(const float* W, const float* LA, const float* LB, co
                             cudaStream_t stream);
 
 // gram.cu (Kronecker factors from samples)
+size_t gram_workspace_bytes(int64_t d, int64_t N, bool weighted);
 cudaError_t gram_launch(const uint16_t* X, int d, int N, int ldx, const float* w, float alpha, float beta, float* G,
-                        int32_t* status_dev, cudaStream_t stream);
+                        void* ws, int32_t* status_dev, cudaStream_t stream);
 cudaError_t sq_norms_launch(const uint16_t* Y, int m, int N, int ldy, float* w, cudaStream_t stream);
 cudaError_t damp_launch(float* G, int d, float rel, cudaStream_t stream);
 

@@ -173,15 +173,21 @@ def test_antidiag_entry_point_rejects_bad_arguments(lib):
 def test_gram_entry_points_reject_bad_arguments(lib):
     X, G, st = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
     w = ctypes.c_void_p(0x4000)
+    ws = ctypes.c_void_p(0x100000)
+    need = lib.bakron_gram_workspace_size(8, 8, 0)
+    assert need == 16384 and lib.bakron_gram_workspace_size(8, 8, 1) == 3 * 16384  # one 128 x 64 block each
+    assert lib.bakron_gram_workspace_size(129, 65, 0) == 4 * 16384
     g = lib.bakron_gram
-    assert g(X, 0, 8, 8, None, 1.0, 0.0, G, st, None) == 1  # d < 1
-    assert g(X, 8, 0, 8, None, 1.0, 0.0, G, st, None) == 1  # N < 1
-    assert g(X, 8, 9, 8, None, 1.0, 0.0, G, st, None) == 1  # ldx < N
-    assert g(X, 8, 6, 6, None, 1.0, 0.0, G, st, None) == 1  # ldx not a multiple of 8
-    assert g(ctypes.c_void_p(0x1008), 8, 8, 8, None, 1.0, 0.0, G, st, None) == 1  # X not 16-byte aligned
-    assert g(X, 8, 8, 8, ctypes.c_void_p(0x4004), 1.0, 0.0, G, st, None) == 1  # w not 16-byte aligned
-    assert g(X, 8, 8, 8, w, 1.0, 0.0, X, st, None) == 1  # G aliases X
-    assert g(X, 8, 8, 8, w, 1.0, 0.0, G, None, None) == 1  # no status word
+    assert g(X, 0, 8, 8, None, 1.0, 0.0, G, ws, need, st, None) == 1  # d < 1
+    assert g(X, 8, 0, 8, None, 1.0, 0.0, G, ws, need, st, None) == 1  # N < 1
+    assert g(X, 8, 9, 8, None, 1.0, 0.0, G, ws, need, st, None) == 1  # ldx < N
+    assert g(X, 8, 6, 6, None, 1.0, 0.0, G, ws, need, st, None) == 1  # ldx not a multiple of 8
+    assert g(ctypes.c_void_p(0x1008), 8, 8, 8, None, 1.0, 0.0, G, ws, need, st, None) == 1  # X not 16-byte aligned
+    assert g(X, 8, 8, 8, ctypes.c_void_p(0x4004), 1.0, 0.0, G, ws, need, st, None) == 1  # w not 16-byte aligned
+    assert g(X, 8, 8, 8, w, 1.0, 0.0, X, ws, 3 * need, st, None) == 1  # G aliases X
+    assert g(X, 8, 8, 8, w, 1.0, 0.0, G, ws, 3 * need, None, None) == 1  # no status word
+    assert g(X, 8, 8, 8, w, 1.0, 0.0, G, ws, 3 * need - 1, st, None) == 4  # weighted needs three copies
+    assert g(X, 8, 8, 8, None, 1.0, 0.0, G, ctypes.c_void_p(0x100010), need, st, None) == 4  # misaligned workspace
     assert lib.bakron_sq_norms(X, 4, 8, 7, w, None) == 1  # ldy < N
     assert lib.bakron_sq_norms(None, 4, 8, 8, w, None) == 1
     assert lib.bakron_damp(None, 4, 0.5, None) == 1
