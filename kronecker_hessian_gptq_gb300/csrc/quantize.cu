@@ -94,11 +94,14 @@ struct QParams {
   int32_t* status;
   const signed char* expA;    // (row, chunk) exponents of L_A and L_B (chunk products)
   const signed char* expB;
+  const __nv_bfloat16* FdA;   // factor digits of L_A and L_B, packed for bulk copies (factor_digits_kernel)
+  const __nv_bfloat16* FdB;
   __nv_bfloat16* DE;          // digits of E, [digit][row][ldE], ldE = n rounded up to 8
   __nv_bfloat16* DGt;         // digits of G transposed, [digit][col][ldG], ldG = m rounded up to 8
   size_t dstrideE, dstrideG;  // elements per digit plane
   int ldE, ldG;
   int m, n, Mt, Nt, bits, lo, hi, nchA, nchB;
+  int ntA, ntB;               // tile rows (32) of the packed factor digits
 };
 
 __device__ __forceinline__ unsigned warp_max(unsigned v) {
@@ -658,8 +661,6 @@ constexpr int kLevels = 6;       // levels 0 .. kDigD - 1
 constexpr int kTcM = 128;        // target rows per group (UC target tiles)
 constexpr int UC = kTcM / T;
 constexpr int kSlab = 32;        // k per slab of factor digits
-constexpr int kTcWarps = 12;
-constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kGroupsPerCta = 8;  // target groups one chunk product CTA works through
 
 // Exponent of every (row, chunk) block of a d x d factor: out[r * nch + c]
@@ -676,6 +677,51 @@ __global__ void __launch_bounds__(256) factor_exp_kernel(const float* F, int d, 
   }
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) out[wid] = (signed char)bound_exp(mx);
+}
+
+// Factor digits, computed once per solve (the factors and their block
+// exponents are fixed for the whole solve): element (row gr, column gk) of a
+// d x d factor, x = F[gr][gk] 2^(7 - e) with e = the block exponent of (gr,
+// chunk gk / CK), is split into kDigF integer digits
+//     x = d_0 + d_1 / 256 + d_2 / 256^2 + ... (each |d_a| <= 128, exact in bf16)
+// by rounding to the nearest integer (ties to even: adding and subtracting
+// 1.5 * 2^23, exact for |u| <= 128.5) and scaling the remainder by 256.
+// Layout: for chunk c, slab s (32 columns), digit a and tile row t (32 rows)
+// one 2 KB block in the tcgen05 core-matrix order of the chunk products'
+// shared memory, offset (r/8) 512 + (k/8) 128 + (r%8) 16 + (k%8) 2, blocks
+// ordered [c][s][a][t]: the four tiles of a target group are 8 contiguous
+// KB, one bulk copy per digit.  Entries outside the matrix are zero.
+// One thread per (c, s, t, row, 8 columns).
+__global__ void __launch_bounds__(256) factor_digits_kernel(const float* F, int d, int nch, int nt,
+                                                            const signed char* fexp, __nv_bfloat16* Fd) {
+  const size_t items = (size_t)nch * (CK / kSlab) * nt * T * (kSlab / 8);
+  for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (size_t)gridDim.x * blockDim.x) {
+    const int k8 = 8 * (int)(it % (kSlab / 8));
+    const int r = (int)((it / (kSlab / 8)) % T);
+    const int t = (int)((it / (kSlab / 8 * T)) % nt);
+    const size_t cs = it / ((size_t)kSlab / 8 * T * nt);  // c * (CK / kSlab) + s
+    const int c = (int)(cs / (CK / kSlab)), sl = (int)(cs % (CK / kSlab));
+    const int gr = t * T + r, gk = c * CK + sl * kSlab + k8;
+    float u[8];
+    const float sc = gr < d ? pow2f(7 - fexp[(size_t)gr * nch + c]) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u[e] = (gr < d && gk + e < d) ? F[(size_t)gr * d + gk + e] * sc : 0.f;
+    const int off = (r / 8) * 512 + (k8 / 8) * 128 + (r % 8) * 16;
+#pragma unroll
+    for (int a = 0; a < kDigF; ++a) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d0 = (u[2 * e] + 0x1.8p23f) - 0x1.8p23f;
+        const float d1 = (u[2 * e + 1] + 0x1.8p23f) - 0x1.8p23f;
+        w[e] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);  // bf16 patterns, low half: smaller k
+        u[2 * e] = (u[2 * e] - d0) * 256.f;  // exact: |u - d| <= 1/2, u has <= 24 significant bits
+        u[2 * e + 1] = (u[2 * e + 1] - d1) * 256.f;
+      }
+      unsigned char* blk = reinterpret_cast<unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t) * 2048;
+      *reinterpret_cast<uint4*>(blk + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
 }
 
 // Chunk product candidates closed by tile anti-diagonal K: for every column
@@ -709,21 +755,44 @@ __device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int nca
   return cc.ntiles > 0;
 }
 
-// -- tcgen05 building blocks.  Operands in shared memory use the canonical
 // Warp roles of a chunk product CTA.
 constexpr int kTcMmaWarp = 0;           // issues the tensor-core products (lane 0)
+constexpr int kTcCopyWarp = 1;          // packed digits: lane 0 loads the factor digit slabs (bulk copies)
 constexpr int kTcEpiWarp0 = 4;          // warps 4..7: epilogue, tensor-memory lane quarters 0..3
-constexpr int kTcProducers = (kTcWarps - 5) * 32;  // warps 1..3 and 8..: factor loads and digits
-constexpr int kTcStages = 3;            // fp32 factor slabs in flight per producer
+constexpr int kTcStages = 3;            // fp32 factor slabs in flight per producer (digits made in the kernel)
 constexpr int kEpiCols = 8;             // output columns per epilogue step (registers: 6 levels each)
-// (16 warps with 11 producers and a 64-register cap were measured no faster.)
 
-struct TcSmem {
+// Two ways to feed the factor digits.  Packed (layers above 2^24 weights):
+// the digits are computed once per solve (factor_digits_kernel) and each
+// slab arrives as five bulk copies, 8 warps.  In the kernel (smaller
+// layers): 7 producer warps copy fp32 factor slabs with cp.async and split
+// them into digits, 12 warps.  Packed reads 10 bytes per factor entry
+// instead of 4 and runs the products faster alone; on 4096 x 4096, where the
+// solve chain and not the products sets the pace, its heavier traffic slowed
+// the chain more than it gained (16.7-17.4 ms against 16.6 ms on one GPU),
+// on 14336 x 4096 it gains 15% (66.8 against 78.6 ms).
+inline bool use_packed_digits(int64_t m, int64_t n) { return m * n > ((int64_t)1 << 24); }
+
+template <bool kPacked>
+struct TcShape {
+  static constexpr int kWarps = kPacked ? 8 : 12;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kProducers = kPacked ? 0 : (kWarps - 5) * 32;  // warps 1..3 and 8..11
+};
+
+template <bool kPacked>
+struct TcStage {
+  float stage[kTcStages][kTcM][kSlab];  // fp32 factor slabs as loaded
+};
+template <>
+struct TcStage<true> {};
+
+template <bool kPacked>
+struct TcSmem : TcStage<kPacked> {
   __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
   __nv_bfloat16 Bd[kDigD * T * CK];         // source digits, 192 rows (digit-major) x CK, SBO 2048 B
-  float stage[kTcStages][kTcM][kSlab];      // fp32 factor slabs as loaded
   int er[kGroupsPerCta][kTcM];              // row exponents of each group's factor block
-  uint64_t full[2];                         // digit slab p written (producer arrivals)
+  uint64_t full[2];                         // digit slab p ready (producer arrivals / bulk-copy bytes)
   uint64_t empty[2];                        // products reading digit slab p done (commit)
   uint64_t grp_full[2];                     // products of a group in tensor-memory half h done (commit)
   uint64_t grp_empty[2];                    // epilogue of tensor-memory half h done (epilogue arrivals)
@@ -737,22 +806,25 @@ struct TcSmem {
 // row products, as their transpose:
 //   Gc[I, targets]^T += L_A[targets, chunk cols] E[I, chunk cols]^T.
 // Warp-specialized pipeline over the k-slabs of all groups of the CTA:
-//  * producers copy fp32 factor slabs two ahead (cp.async, each thread its
-//    own items) and turn them into digits in one of two digit buffers, once
-//    the products that read that buffer are done;
+//  * the next slab's five factor digit blocks go into one of two digit
+//    buffers once the products that read that buffer are done: bulk copies
+//    of the packed digits by one thread, or fp32 slabs copied two ahead
+//    (cp.async) by the producer warps and split into digits there;
 //  * one thread issues, per 16-deep k-step, five MMAs: factor digit a times
 //    the source digits 0 .. 5-a stacked along N (N = 32 (6 - a)), written at
 //    tensor-memory column 32 a, so the block of source digit b lands on
 //    level a + b: the 20 digit pairs in five products;
-//  * epilogue warps turn each finished group's six levels into double-float
+//  * epilogue warps turn each finished group's six levels into fixed-point
 //    updates of the plane, while the next group is multiplied in the other
 //    tensor-memory half.
 // Handshakes are mbarriers; every wait is bounded.
 // (At most 80 registers: 30 K registers, so that a tile solve fits beside
 // it; its shared memory admits one per SM.)
+template <bool kPacked>
 __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col) {
+  using Shape = TcShape<kPacked>;
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(tc_smem_raw);
+  TcSmem<kPacked>& sm = *reinterpret_cast<TcSmem<kPacked>*>(tc_smem_raw);
   ChunkCand cc;
   if (!chunk_candidate(P, K, ncand_col, blockIdx.x, cc)) return;
   const int ngroups = (cc.ntiles + UC - 1) / UC;
@@ -760,58 +832,66 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
   if (g0 >= ngroups) return;
   const int mygroups = min(kGroupsPerCta, (ngroups - 1 - g0) / gstep + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  static_assert(Shape::kWarps >= kTcEpiWarp0 + 4 && kTcCopyWarp < kTcEpiWarp0,
+                "warp roles: MMA, copies or producers, 4 epilogue warps");
   const bool is_epi = warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4;
-  const bool is_prod = warp != kTcMmaWarp && !is_epi;
-  const int ptid = is_prod ? (warp < kTcEpiWarp0 ? tid - 32 : tid - 160) : -1;  // 0 .. kTcProducers-1
-  static_assert(kTcWarps >= 9, "warp roles: 1 MMA + 4 epilogue + producers");
+  const bool is_prod = !kPacked && warp != kTcMmaWarp && !is_epi;
+  const int ptid = is_prod ? (warp < kTcEpiWarp0 ? tid - 32 : tid - 160) : -1;  // 0 .. kProducers-1
   const float* F = cc.col ? P.LB : P.LA;
+  const __nv_bfloat16* Fd = cc.col ? P.FdB : P.FdA;
+  const int nt = cc.col ? P.ntB : P.ntA;
   const signed char* fexp = cc.col ? P.expB : P.expA;
   const int d = cc.col ? P.m : P.n;
   const int nch = cc.col ? P.nchB : P.nchA;
   constexpr int nslab = CK / kSlab;
   const int nz = mygroups * nslab;  // slabs of all groups, in order
-  const bool vec4 = (d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0;
   auto group_row0 = [&](int gi) { return (cc.first + (g0 + gi * gstep) * UC) * T; };
   auto group_rows = [&](int gi) { return min(kTcM, (cc.first + cc.ntiles) * T - group_row0(gi)); };
 
   // Producer item it (of kTcM * kSlab / 8): row it / 4, columns 8 (it mod 4) .. +7.
   auto copy_slab = [&](int z) {
-    if (z < nz) {
-      const int gi = z / nslab, s = z % nslab;
-      const int row0 = group_row0(gi), rows = group_rows(gi);
-      for (int it = ptid; it < kTcM * kSlab / 8; it += kTcProducers) {
-        const int r = it / 4, k8 = 8 * (it % 4);
-        const int gr = row0 + r, gk = cc.c * CK + s * kSlab + k8;
-        const bool rok = r < rows && gr < d;
-        float* dst = &sm.stage[z % kTcStages][r][k8];
-        const float* src = F + (size_t)(rok ? gr : 0) * d;
-        if (vec4) {
+    if constexpr (!kPacked) {
+      const bool vec4 = (d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0;
+      if (z < nz) {
+        const int gi = z / nslab, s = z % nslab;
+        const int row0 = group_row0(gi), rows = group_rows(gi);
+        for (int it = ptid; it < kTcM * kSlab / 8; it += Shape::kProducers) {
+          const int r = it / 4, k8 = 8 * (it % 4);
+          const int gr = row0 + r, gk = cc.c * CK + s * kSlab + k8;
+          const bool rok = r < rows && gr < d;
+          float* dst = &sm.stage[z % kTcStages][r][k8];
+          const float* src = F + (size_t)(rok ? gr : 0) * d;
+          if (vec4) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const bool ok = rok && gk + 4 * h < d;
-            cp_async(dst + 4 * h, ok ? (const void*)(src + gk + 4 * h) : (const void*)F, ok ? 16 : 0, 16);
-          }
-        } else {
+            for (int h = 0; h < 2; ++h) {
+              const bool ok = rok && gk + 4 * h < d;
+              cp_async(dst + 4 * h, ok ? (const void*)(src + gk + 4 * h) : (const void*)F, ok ? 16 : 0, 16);
+            }
+          } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const bool ok = rok && gk + e < d;
-            cp_async(dst + e, ok ? (const void*)(src + gk + e) : (const void*)F, ok ? 4 : 0, 4);
+            for (int e = 0; e < 8; ++e) {
+              const bool ok = rok && gk + e < d;
+              cp_async(dst + e, ok ? (const void*)(src + gk + e) : (const void*)F, ok ? 4 : 0, 4);
+            }
           }
         }
       }
+      cp_async_commit();  // one group per slab, empty past the end, so that the counts stay uniform
     }
-    cp_async_commit();  // one group per slab, empty past the end, so that the counts stay uniform
   };
 
-  // Prologue: source digits (written by the tile solves) with all producer
-  // threads, row exponents, mbarriers, tensor memory; the first two slabs.
-  if (is_prod) {
+  // Prologue: source digits (written by the tile solves; by all threads, or
+  // by the producers), row exponents, mbarriers, tensor memory; without
+  // packed digits also the first two fp32 slabs.
+  const int copier = kPacked ? tid : ptid;
+  const int ncopiers = kPacked ? Shape::kThreads : Shape::kProducers;
+  if (copier >= 0) {
     const __nv_bfloat16* dp = cc.col ? P.DGt : P.DE;
     const size_t pst = cc.col ? P.dstrideG : P.dstrideE;
     const int ld = cc.col ? P.ldG : P.ldE;
     const int qlim = cc.col ? P.n : P.m, klim = cc.col ? P.m : P.n;
     const int q0 = cc.col ? cc.J * T : cc.I * T;
-    for (int e = ptid; e < kDigD * T * (CK / 8); e += kTcProducers) {
+    for (int e = copier; e < kDigD * T * (CK / 8); e += ncopiers) {
       const int b = e / (T * (CK / 8));
       const int q = (e / (CK / 8)) % T;
       const int k8 = 8 * (e % (CK / 8));
@@ -834,18 +914,21 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
   if (tid == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])), "r"(kTcProducers));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])),
+                   "r"(kPacked ? 1 : Shape::kProducers));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.grp_full[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.grp_empty[i])));
     }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == kTcMmaWarp) {  // two tensor-memory halves of 256 columns (6 levels x 32 used in each)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(&sm.tmem_base)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
-  if (is_prod) {
-    asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // the source digits (slabs 0, 1 may be in flight)
+  if (copier >= 0) {
+    // the source digits (without packed digits slabs 0, 1 may be in flight)
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kPacked ? 0 : 2) : "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   }
   tc_fence_before();
@@ -855,41 +938,69 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
   const int eD = bound_exp(P.hdr->sigma);
   bool broken = false;
 
-  if (is_prod) {
-    for (int z = 0; z < nz; ++z) {
-      const int p = z & 1, gi = z / nslab;
-      copy_slab(z + 2);
-      asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // this thread's items of slab z
-      if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
-      for (int it = ptid; it < kTcM * kSlab / 8; it += kTcProducers) {
-        const int r = it / 4, k8 = 8 * (it % 4);
-        const float sc = pow2f(7 - sm.er[gi][r]);
-        const float4 x0 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8]);
-        const float4 x1 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8 + 4]);
-        float u[8] = {x0.x * sc, x0.y * sc, x0.z * sc, x0.w * sc, x1.x * sc, x1.y * sc, x1.z * sc, x1.w * sc};
-        const int off = (r / 8) * 512 + (k8 / 8) * 128 + (r % 8) * 16;
+  if (kPacked ? warp == kTcCopyWarp : is_prod) {
+    if constexpr (kPacked) {
+      if (lane == 0) {
+        // Slab z of group gi: for each digit a, the group's tiles (at most
+        // UC) are contiguous 2 KB blocks of the packed digits: one bulk copy.
+        for (int z = 0; z < nz; ++z) {
+          const int p = z & 1, gi = z / nslab, s = z % nslab;
+          const int t0 = group_row0(gi) / T;
+          const int ntg = min(UC, nt - t0);
+          const uint32_t bytes = (uint32_t)ntg * 2048u;
+          if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+          if (broken) break;
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[p])),
+                       "r"(bytes * kDigF)
+                       : "memory");
+          const size_t cs = (size_t)cc.c * nslab + s;
 #pragma unroll
-        for (int a = 0; a < kDigF; ++a) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // Round to the nearest integer (ties to even) by adding and
-            // subtracting 1.5 * 2^23 (|u| <= 128.5: exact), on the fp32 pipes.
-            // The integer, of at most 8 significant bits, is exact in bf16:
-            // its bf16 pattern is the upper half of its fp32 pattern, and one
-            // byte permute packs two of them (low half: the smaller k).
-            const float d0 = (u[2 * e] + 0x1.8p23f) - 0x1.8p23f;
-            const float d1 = (u[2 * e + 1] + 0x1.8p23f) - 0x1.8p23f;
-            w[e] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
-            u[2 * e] = (u[2 * e] - d0) * 256.f;  // exact: |u - d| <= 1/2, u has <= 24 significant bits
-            u[2 * e + 1] = (u[2 * e + 1] - d1) * 256.f;
+          for (int a = 0; a < kDigF; ++a) {
+            const unsigned char* src =
+                reinterpret_cast<const unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t0) * 2048;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                    smem_u32(sm.A[p][a])),
+                "l"(src), "r"(bytes), "r"(smem_u32(&sm.full[p]))
+                : "memory");
           }
-          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(sm.A[p][a]) + off) =
-              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[p])) : "memory");
+      __syncwarp();
+    } else {
+      for (int z = 0; z < nz; ++z) {
+        const int p = z & 1, gi = z / nslab;
+        copy_slab(z + 2);
+        asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // this thread's items of slab z
+        if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+        for (int it = ptid; it < kTcM * kSlab / 8; it += Shape::kProducers) {
+          const int r = it / 4, k8 = 8 * (it % 4);
+          const float sc = pow2f(7 - sm.er[gi][r]);
+          const float4 x0 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8]);
+          const float4 x1 = *reinterpret_cast<const float4*>(&sm.stage[z % kTcStages][r][k8 + 4]);
+          float u[8] = {x0.x * sc, x0.y * sc, x0.z * sc, x0.w * sc, x1.x * sc, x1.y * sc, x1.z * sc, x1.w * sc};
+          const int off = (r / 8) * 512 + (k8 / 8) * 128 + (r % 8) * 16;
+#pragma unroll
+          for (int a = 0; a < kDigF; ++a) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // The same digit split as factor_digits_kernel (round to the
+              // nearest integer by adding and subtracting 1.5 * 2^23, bf16
+              // pattern = the fp32 pattern's upper half, two per word).
+              const float d0 = (u[2 * e] + 0x1.8p23f) - 0x1.8p23f;
+              const float d1 = (u[2 * e + 1] + 0x1.8p23f) - 0x1.8p23f;
+              w[e] = __byte_perm(__float_as_uint(d0), __float_as_uint(d1), 0x7632);
+              u[2 * e] = (u[2 * e] - d0) * 256.f;
+              u[2 * e + 1] = (u[2 * e + 1] - d1) * 256.f;
+            }
+            *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(sm.A[p][a]) + off) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[p])) : "memory");
+      }
     }
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) {
@@ -897,6 +1008,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
         const int p = z & 1, gi = z / nslab, s = z % nslab, h = gi & 1;
         if (s == 0 && gi >= 2) mbar_wait(&sm.grp_empty[h], (uint32_t)((gi >> 1) - 1) & 1u, broken);
         mbar_wait(&sm.full[p], (uint32_t)(z >> 1) & 1u, broken);
+        if (broken) break;
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < kSlab / 16; ++j) {
@@ -913,7 +1025,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
       }
     }
     __syncwarp();
-  } else {  // epilogue warps
+  } else if (warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4) {  // epilogue warps
     const int qd = warp - kTcEpiWarp0;  // tensor-memory lane quarter
     const int r = 32 * qd + lane;       // output row of this thread within the group
     for (int gi = 0; gi < mygroups; ++gi) {
@@ -1028,10 +1140,12 @@ class LaunchClock {
 // Calls that share a set serialize their side work on its streams, which
 // is correct: each call's main stream waits only on its own events' records.
 // Dynamic shared memory: a mid push CTA holds one stage; a chunk product
-// CTA the source digits, two factor digit slabs and three fp32 factor slabs
-// (178 KB: one per SM, with room beside it for a tile solve).
+// CTA the source digits, two factor digit slabs and, when it makes the
+// digits itself, three fp32 factor slabs (178 KB, else 130 KB: one per SM,
+// with room beside it for a tile solve).
 constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
-constexpr int kChunkSmem = (int)sizeof(TcSmem);
+template <bool kPacked>
+constexpr int kChunkSmem = (int)sizeof(TcSmem<kPacked>);
 
 // Chunk launches of consecutive tile anti-diagonals go round-robin over
 // kChunkStreams streams.  With more than one they overlap and may update
@@ -1066,7 +1180,10 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
       e = cudaStreamCreateWithPriority(&S.chunk[i], cudaStreamNonBlocking, hi);
       if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
+    e = cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kChunkSmem<false>);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem<true>);
     if (e != cudaSuccess) return e;
     S.ready = true;
   }
@@ -1084,7 +1201,7 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
 // Workspace: header, the six planes, the factor exponents, the source
 // digits of E and G.
 struct WsLayout {
-  size_t plane, expA, expB, DE, DG, dplaneE, dplaneG, total;
+  size_t plane, expA, expB, DE, DG, dplaneE, dplaneG, FdA, FdB, total;
   int ldE, ldG;
 };
 WsLayout ws_layout(int64_t m, int64_t n) {
@@ -1104,6 +1221,14 @@ WsLayout ws_layout(int64_t m, int64_t n) {
   off += kDigD * L.dplaneE;
   L.DG = off;
   off += kDigD * L.dplaneG;
+  // packed factor digits (layers above 2^24 weights): nch chunks x
+  // (CK / kSlab) slabs x kDigF digits x nt tiles x 2 KB per factor
+  const bool packed = use_packed_digits(m, n);
+  const size_t ntA = (size_t)((n + T - 1) / T), ntB = (size_t)((m + T - 1) / T);
+  L.FdA = off;
+  if (packed) off += align_up(nchA * (CK / kSlab) * kDigF * ntA * 2048);
+  L.FdB = off;
+  if (packed) off += align_up(nchB * (CK / kSlab) * kDigF * ntB * 2048);
   L.total = off;
   return L;
 }
@@ -1114,6 +1239,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
   const WsLayout lay = ws_layout(m, n);
+  const bool packed = use_packed_digits(m, n);
   const size_t plane = lay.plane;
   char* base = static_cast<char*>(ws);
   float2* planes = reinterpret_cast<float2*>(base + sizeof(Header));
@@ -1146,6 +1272,10 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   P.ldG = lay.ldG;
   P.nchA = (n + CK - 1) / CK;
   P.nchB = (m + CK - 1) / CK;
+  P.ntA = (n + T - 1) / T;
+  P.ntB = (m + T - 1) / T;
+  P.FdA = reinterpret_cast<const __nv_bfloat16*>(base + lay.FdA);
+  P.FdB = reinterpret_cast<const __nv_bfloat16*>(base + lay.FdB);
   P.m = m;
   P.n = n;
   P.Mt = (m + T - 1) / T;
@@ -1193,6 +1323,14 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     const size_t wA = (size_t)n * P.nchA, wB = (size_t)m * P.nchB;  // one warp per (row, chunk)
     factor_exp_kernel<<<(unsigned)((wA + 7) / 8), 256, 0, stream>>>(LA, n, P.nchA, eA);
     if (LB) factor_exp_kernel<<<(unsigned)((wB + 7) / 8), 256, 0, stream>>>(LB, m, P.nchB, eB);
+    if (packed) {  // the factors' digits, once per solve, for the chunk products' bulk copies
+      const int digit_blocks = 152 * 8;
+      factor_digits_kernel<<<digit_blocks, 256, 0, stream>>>(LA, n, P.nchA, P.ntA, eA,
+                                                             const_cast<__nv_bfloat16*>(P.FdA));
+      if (LB)
+        factor_digits_kernel<<<digit_blocks, 256, 0, stream>>>(LB, m, P.nchB, P.ntB, eB,
+                                                               const_cast<__nv_bfloat16*>(P.FdB));
+    }
   }
   clock.end(0.0);
   cudaEventRecord(ev_start, stream);
@@ -1263,7 +1401,12 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
       const int groups = (chunk_most + UC - 1) / UC;
       const int ctas = (groups + kGroupsPerCta - 1) / kGroupsPerCta;  // CTAs per candidate
       clock.begin(3, s_chunk(K));
-      chunk_tc_kernel<<<dim3(ncc + ncr, ctas), kTcThreads, kChunkSmem, s_chunk(K)>>>(P, K, ncc);
+      if (packed)
+        chunk_tc_kernel<true><<<dim3(ncc + ncr, ctas), TcShape<true>::kThreads, kChunkSmem<true>, s_chunk(K)>>>(
+            P, K, ncc);
+      else
+        chunk_tc_kernel<false><<<dim3(ncc + ncr, ctas), TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
+            P, K, ncc);
       clock.end(2.0 * B * t3 * chunk_tiles);
       cudaEventRecord(ev_chunk[K], s_chunk(K));
       chunk_on[K] = 1;
