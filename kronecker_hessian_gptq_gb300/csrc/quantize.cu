@@ -102,6 +102,10 @@ struct QParams {
   int ldE, ldG;
   int m, n, Mt, Nt, bits, lo, hi, nchA, nchB;
   int ntA, ntB;               // tile rows (32) of the packed factor digits
+  // Step of tile (I, J): J + skew I.  skew = 1 (BaKron): tile anti-diagonals;
+  // skew = 0 (L_B = I, row-wise GPTQ): tile columns, all rows at once, since
+  // a row then depends on nothing but its own earlier entries.
+  int skew;
 };
 
 __device__ __forceinline__ unsigned warp_max(unsigned v) {
@@ -227,7 +231,8 @@ __device__ __forceinline__ float2 df_from_fixed(long long v, float from_units) {
 // s + 2 .. mid_end(s) - 1; the chunk product covers targets >= mid_end(s).
 __host__ __device__ __forceinline__ int mid_end(int s) { return (s / B + 2) * B; }
 
-// Solves every tile (I, K - I), I = I0 + blockIdx.x, of tile anti-diagonal K.
+// Solves every tile (I, K - skew I), I = I0 + blockIdx.x, of step K (a tile
+// anti-diagonal, or with L_B = I a tile column).
 // 512 threads; lane p owns the two entries (p, q_j) of tile row p with
 // p + q_j = 2 w + j (mod 32), j = 0, 1, w the warp: the entries of one
 // anti-diagonal sit in one warp and one slot j, so only that warp runs the
@@ -238,7 +243,7 @@ constexpr int kRows = kSolveThreads / T;     // rows per pass of the natural map
 
 __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, int K, int I0) {
   const int I = I0 + blockIdx.x;
-  const int J = K - I;
+  const int J = K - P.skew * I;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float2 zero = make_float2(0.f, 0.f);
 
@@ -612,12 +617,13 @@ __device__ void row_push(const QParams& P, PushSmem<NS>& sm, float2* Gp, int I, 
     }
 }
 
-// Mid pushes of the sources of tile anti-diagonal K (blockIdx.x: source
-// I = I0 + blockIdx.x; blockIdx.y: group of U targets, column targets first).
+// Mid pushes of the sources of step K (blockIdx.x: source I = I0 +
+// blockIdx.x, J = K - skew I; blockIdx.y: group of U targets, column
+// targets first).
 __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0) {
   extern __shared__ __align__(16) unsigned char push_smem[];
   PushSmem<1>& sm = *reinterpret_cast<PushSmem<1>*>(push_smem);
-  const int I = I0 + blockIdx.x, J = K - I;
+  const int I = I0 + blockIdx.x, J = K - P.skew * I;
   const int c_first = I + 2, c_end = P.LB ? min(P.Mt, mid_end(I)) : c_first;  // L_B = I: no column pushes
   const int r_first = J + 2, r_end = min(P.Nt, mid_end(J));
   const int ncu = c_end > c_first ? (c_end - c_first + U - 1) / U : 0;
@@ -743,6 +749,15 @@ __device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int nca
     cc.c = last / B;
     cc.first = (cc.c + 2) * B;
     cc.ntiles = P.Mt - cc.first;
+  } else if (P.skew == 0) {
+    // tile columns: every row closes a chunk of B tile columns together
+    cc.I = t - ncand_col;
+    cc.J = 0;
+    const int last = K;
+    if ((K + 1) % B != 0 || cc.I >= P.Mt || last >= P.Nt) return false;
+    cc.c = last / B;
+    cc.first = (cc.c + 2) * B;
+    cc.ntiles = P.Nt - cc.first;
   } else {
     cc.I = K - (B - 1) - B * (t - ncand_col);
     cc.J = 0;
@@ -1274,6 +1289,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   P.nchB = (m + CK - 1) / CK;
   P.ntA = (n + T - 1) / T;
   P.ntB = (m + T - 1) / T;
+  P.skew = LB ? 1 : 0;
   P.FdA = reinterpret_cast<const __nv_bfloat16*>(base + lay.FdA);
   P.FdB = reinterpret_cast<const __nv_bfloat16*>(base + lay.FdB);
   P.m = m;
@@ -1283,7 +1299,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   P.bits = al.bounded ? 1 : 0;  // 1: the codes are clamped to {lo .. hi}
   P.lo = al.lo;
   P.hi = al.hi;
-  const int Kmax = P.Mt + P.Nt - 2;
+  const int Kmax = P.skew ? P.Mt + P.Nt - 2 : P.Nt - 1;
 
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -1343,8 +1359,8 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   int last_chunk[kChunkStreams];
   for (int i = 0; i < kChunkStreams; ++i) last_chunk[i] = -1;
   for (int K = 0; K <= Kmax; ++K) {
-    const int I0 = std::max(0, K - (P.Nt - 1));
-    const int I1 = std::min(K, P.Mt - 1);
+    const int I0 = P.skew ? std::max(0, K - (P.Nt - 1)) : 0;
+    const int I1 = P.skew ? std::min(K, P.Mt - 1) : P.Mt - 1;
     const int nsrc = I1 - I0 + 1;
     if (K >= 2 && mid_on[K - 2]) cudaStreamWaitEvent(stream, ev_mid[K - 2], 0);
     // One wait each is enough: mid(K-2) follows every earlier mid launch on
@@ -1360,7 +1376,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     // mid pushes from the sources of K
     double mid_tiles = 0;
     for (int I = I0; I <= I1; ++I) {
-      const int J = K - I;
+      const int J = K - P.skew * I;
       if (LB) mid_tiles += std::max(0, std::min(P.Mt, mid_end(I)) - (I + 2));
       mid_tiles += std::max(0, std::min(P.Nt, mid_end(J)) - (J + 2));
     }
@@ -1377,7 +1393,8 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
 
     // chunk products closed by K
     const int ncc = (LB && std::min(K, P.Mt - 1) >= B - 1) ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
-    const int ncr = std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0;
+    const int ncr = P.skew ? (std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0)
+                           : ((K + 1) % B == 0 ? P.Mt : 0);  // tile columns: every row closes a chunk
     double chunk_tiles = 0;
     int chunk_most = 0;  // most targets of one candidate
     for (int t = 0; t < ncc; ++t) {
@@ -1389,7 +1406,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
       }
     }
     for (int t = 0; t < ncr; ++t) {
-      const int I = K - (B - 1) - B * t, last = K - I;
+      const int I = P.skew ? K - (B - 1) - B * t : t, last = K - P.skew * I;
       if (I >= 0 && I < P.Mt && last < P.Nt) {
         const int nt = std::max(0, P.Nt - (last / B + 2) * B);
         chunk_tiles += nt;
