@@ -574,6 +574,8 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32x2 double-float; bf16 digit products on tensor cores", "data": "synthetic",
         "config": workload_config(p, world),
         "solve_alg_tflops": f_alg / (total_ms / args.steps * 1e-3) / 1e12,
+        # the solve is a chain of m + n - 1 anti-diagonal steps; on small layers the chain sets the time
+        "us_per_antidiagonal_step": total_ms / args.steps * 1e3 / (m + n - 1),
         "prep_ms": prep_ms,
         "roofline": roof,
         "kernels": kernels,
