@@ -220,13 +220,20 @@ KERNEL_SOURCES = ("kronecker_hessian_gptq_gb300/csrc/quantize.cu", "kronecker_he
 
 
 def kernel_source_digest() -> str:
-    """sha256 over the sources the solve kernels are compiled from."""
+    """sha256 over the code of the sources the solve kernels are compiled
+    from: comments removed and whitespace collapsed, so that an edit of a
+    comment does not void a traffic measurement of unchanged code."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(rel.encode())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

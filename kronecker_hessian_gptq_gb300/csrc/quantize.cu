@@ -27,6 +27,9 @@
 //           in chunk c pushes itself to the targets before chunk c+2; the
 //           chunk product covers the targets from chunk c+2 on, so it has
 //           B+1 tile anti-diagonals of slack and runs off the critical path.
+// With L_B = I (row-wise GPTQ) only the row part exists, a tile depends on
+// nothing but the earlier tiles of its own tile row, and a step K is a whole
+// tile column J = K (QParams::skew = 0) instead of a tile anti-diagonal.
 // Streams: the caller's stream runs the tile solves, a second one the mid
 // pushes, a third one the chunk products; events order
 //   solve(K) -> mid(K) -> solve(K+2)   and   solve(K) -> chunk(K) -> solve(K+B+1).

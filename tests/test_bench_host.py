@@ -100,8 +100,11 @@ def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
         f"# summary\ntraffic_bytes_per_launch: 123456\nsource_sha256: {digest}\n")
     assert bench.profiled_traffic("chunk_push", "c3") == 123456
     with open(tmp_path / bench.KERNEL_SOURCES[0], "a") as f:
-        f.write("\n// edited\n")
-    assert bench.profiled_traffic("chunk_push", "c3") is None  # stale once the kernel changes
+        f.write("\n// a comment edited\n/* and\n another */\n")
+    assert bench.profiled_traffic("chunk_push", "c3") == 123456  # comments do not change the code
+    with open(tmp_path / bench.KERNEL_SOURCES[0], "a") as f:
+        f.write("\nstatic int edited = 1;\n")
+    assert bench.profiled_traffic("chunk_push", "c3") is None  # stale once the code changes
 
 
 def test_roofline_tensor_and_alu_classes():
