@@ -7,6 +7,18 @@ fallback: if the library is missing, every call raises.
 
 Source of the method: "BaKron: Efficient Quantization with Kronecker-Factored
 Hessians" (arXiv 2608.06291), Sec. 3.
+
+The calls, each a C ABI entry point of the same name with the prefix bakron_:
+  factor, prepare        normalized inverse Cholesky factors L-hat (Sec. 3.2)
+  quantize               the BaKron solve (Sec. 3.5, App. B eq. (2))
+  quantize_host          the same from and to host memory
+  gptq                   the one-sided case B = I (row-wise GPTQ, Sec. 1, Alg. 1)
+  antidiag               BaKron-antidiagonal (Sec. 3.2, Alg. 3), the quartic baseline
+  quantize_range         any integer alphabet {lo .. hi} (Sec. 3.1)
+  quantize_scaled        per-run (group) and per-column scales (Sec. 3.1)
+  row_scales             App. D scale choice with the MSE shrink search
+  pack_codes             b-bit packed codes
+  gram, sq_norms, damp   Kronecker factors from samples (Sec. 4.2, App. A.2, App. D)
 """
 
 from __future__ import annotations
