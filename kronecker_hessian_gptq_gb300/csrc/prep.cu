@@ -10,8 +10,9 @@
 // H' = J H J = C~ D C~^T (LDL^T, C~ unit lower); then R = J (C~ D^1/2)^T J and
 // L-hat = J C~^-T J, i.e.  L-hat[i][j] = (C~^-1)[d-1-j][d-1-i].
 // Steps: (1) blocked right-looking LDL^T of H' in 32-column panels
-// (diagonal block, panel solve, trailing update), (2) blocked inverse of the
-// unit lower C~ (diagonal blocks, then block sub-diagonals s = 1, 2, ...),
+// (diagonal block and its inverse, panel as a product with that inverse,
+// trailing update), (2) inverse of the unit lower C~ (block doubling from
+// the diagonal blocks' inverses: 32 -> 64 -> ... rows),
 // (3) the index flip and one rounding to fp32.
 //
 // All arithmetic is double-float (df.cuh).  A pivot d_j <= 0 writes
@@ -51,9 +52,12 @@ __global__ void init_kernel(FParams F) {
   }
 }
 
-// LDL^T of the diagonal block kb in place (one CTA of NB x NB threads).
+// LDL^T of the diagonal block kb in place (one CTA of NB x NB threads), then
+// the inverse W = C~_kk^-1 of its unit lower factor into X's diagonal block
+// (the panel below uses it, and it is the leaf of the inverse of C~).
 __global__ void __launch_bounds__(NB* NB) diag_factor_kernel(FParams F, int kb) {
   __shared__ float2 blk[NB][NB + 1];
+  __shared__ float2 Ws[NB][NB + 1];
   __shared__ float2 col[NB];   // l_ij = a_ij / d_j for the current j
   __shared__ float2 wcol[NB];  // a_ij (= l_ij d_j) for the current j
   const int i = threadIdx.y, l = threadIdx.x;
@@ -75,36 +79,51 @@ __global__ void __launch_bounds__(NB* NB) diag_factor_kernel(FParams F, int kb) 
     __syncthreads();
   }
   if (i < bs && l < bs && l <= i) F.M[(size_t)(base + i) * F.d + base + l] = blk[i][l];
+  // Column c of W by forward substitution (one thread per column, each
+  // touching only its own column of Ws): W[c][c] = 1,
+  // W[r][c] = -sum_{t = c}^{r-1} C~[r][t] W[t][c].
+  if (i == 0 && l < bs) {
+    const int c = l;
+    for (int r = 0; r < NB; ++r) Ws[r][c] = make_float2(r == c ? 1.f : 0.f, 0.f);
+    for (int r = c + 1; r < bs; ++r) {
+      float2 acc = make_float2(0.f, 0.f);
+      for (int t = c; t < r; ++t) acc = df_add(acc, df_mul(blk[r][t], Ws[t][c]));
+      Ws[r][c] = df_neg(acc);
+    }
+  }
+  __syncthreads();
+  if (i < bs && l < bs) F.X[(size_t)(base + i) * F.d + base + l] = Ws[i][l];
 }
 
-// Panel below the diagonal block: row r gets x = a_r C~_kk^-T (forward
-// substitution), stores x in P (= C~_rk D_k) and x D_k^-1 in M (= C~_rk).
-__global__ void __launch_bounds__(128) panel_kernel(FParams F, int kb) {
-  __shared__ float2 Ckk[NB][NB + 1];
+// Panel below the diagonal block: row r's entries a (after the trailing
+// updates of the earlier panels) satisfy C~_kk x = a with x = C~_rk D_k, so
+// x = W a with W = C~_kk^-1 (written by diag_factor_kernel):
+//     x_j = sum_{t <= j} W[j][t] a_t,
+// one double-float dot product per (row, j), all in parallel.  Stores x in
+// P (= C~_rk D_k) and x D_k^-1 in M (= C~_rk).  8 rows per CTA.
+constexpr int kPanelRows = 8;
+__global__ void __launch_bounds__(kPanelRows * NB) panel_kernel(FParams F, int kb) {
+  __shared__ float2 Wk[NB][NB + 1];
+  __shared__ float2 arow[kPanelRows][NB + 1];
+  __shared__ float2 dk[NB];
   const int base = kb * NB;
   const int bs = min(NB, F.d - base);
   for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
     const int a = e / NB, b = e % NB;
-    Ckk[a][b] = (a < bs && b < bs) ? F.M[(size_t)(base + a) * F.d + base + b] : make_float2(0.f, 0.f);
+    Wk[a][b] = (a < bs && b < bs) ? F.X[(size_t)(base + a) * F.d + base + b] : make_float2(0.f, 0.f);
   }
+  if (threadIdx.x < NB)
+    dk[threadIdx.x] = threadIdx.x < bs ? F.M[(size_t)(base + threadIdx.x) * F.d + base + threadIdx.x]
+                                       : make_float2(1.f, 0.f);
+  const int rr = threadIdx.x / NB, j = threadIdx.x % NB;
+  const int r = base + bs + blockIdx.x * kPanelRows + rr;
+  arow[rr][j] = (r < F.d && j < bs) ? F.M[(size_t)r * F.d + base + j] : make_float2(0.f, 0.f);
   __syncthreads();
-  const int r = base + bs + blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= F.d) return;
-  float2 x[NB];
-#pragma unroll
-  for (int j = 0; j < NB; ++j) x[j] = (j < bs) ? F.M[(size_t)r * F.d + base + j] : make_float2(0.f, 0.f);
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-#pragma unroll
-    for (int t = 0; t < j; ++t) x[j] = df_sub(x[j], df_mul(x[t], Ckk[j][t]));
-  }
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-    if (j < bs) {
-      F.P[(size_t)r * NB + j] = x[j];
-      F.M[(size_t)r * F.d + base + j] = df_div(x[j], Ckk[j][j]);
-    }
-  }
+  if (r >= F.d || j >= bs) return;
+  float2 x = make_float2(0.f, 0.f);
+  for (int t = 0; t <= j; ++t) x = df_add(x, df_mul(Wk[j][t], arow[rr][t]));
+  F.P[(size_t)r * NB + j] = x;
+  F.M[(size_t)r * F.d + base + j] = df_div(x, dk[j]);
 }
 
 __device__ __forceinline__ void tri_decode(int t, int& a, int& b) {
@@ -181,58 +200,51 @@ __global__ void __launch_bounds__(256) trailing_kernel(FParams F, int kb) {
   }
 }
 
-// X_kk = C~_kk^-1 for every diagonal block (unit lower), one CTA per block,
-// one thread per column.
-__global__ void __launch_bounds__(NB) inv_diag_kernel(FParams F) {
-  __shared__ float2 C[NB][NB + 1];
-  const int kb = blockIdx.x;
-  const int base = kb * NB;
-  const int bs = min(NB, F.d - base);
-  for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
-    const int a = e / NB, b = e % NB;
-    C[a][b] = (a < bs && b < bs) ? F.M[(size_t)(base + a) * F.d + base + b] : make_float2(0.f, 0.f);
-  }
-  __syncthreads();
-  const int c = threadIdx.x;
-  if (c >= bs) return;
-  float2 x[NB];
-#pragma unroll
-  for (int i = 0; i < NB; ++i) x[i] = make_float2(i == c ? 1.f : 0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    if (i > c) {
-      float2 s = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int t = 0; t < i; ++t)
-        if (t >= c) s = df_add(s, df_mul(C[i][t], x[t]));
-      x[i] = df_neg(s);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NB; ++i)
-    if (i < bs) F.X[(size_t)(base + i) * F.d + base + c] = x[i];
-}
-
-// Block sub-diagonal s of X = C~^-1: for jb, ib = jb + s,
-//   X[ib][jb] = -X[ib][ib] * sum_{kb=jb}^{ib-1} C~[ib][kb] X[kb][jb].
-__global__ void __launch_bounds__(256) inv_offdiag_kernel(FParams F, int s) {
+// X = C~^-1 by block doubling.  For two consecutive diagonal blocks of b
+// rows whose inverses X11, X22 are known (lower triangular),
+//     X21 = -X22 C~21 X11,
+// so the inverses of blocks of 2b follow from those of b in two products.
+// Level b (32, 64, ...) runs every pair of blocks at once, as two launches:
+//   stage 0:  T = C~21 X11     (stored transposed in the unused upper
+//             triangle of X, at rows r1 .., columns r2 .., i.e. X[r1 + j][r2 + i])
+//   stage 1:  X21 = -X22 T.
+// The triangular operand is read with its upper part masked (that part of X
+// holds the scratch T of inner levels), and its zero half skipped: stage 0
+// sums over k >= the tile's first column, stage 1 over k <= its last row.
+// blockIdx.y: pair t (r1 = 2 t b, r2 = r1 + b); blockIdx.x: 32 x 32 output
+// tile (ti, tj), ti over the rows of the second block, tj over the columns
+// of the first.  Each 32-deep chunk is summed on an offset of its own and
+// folded into a double-float total.
+__global__ void __launch_bounds__(256) inv_level_kernel(FParams F, int b, int stage) {
   __shared__ float2 sA[NB][NB + 1];
   __shared__ float2 sB[NB][NB + 1];
-  __shared__ float2 sS[NB][NB + 1];
   __shared__ unsigned red[16];
-  const int jb = blockIdx.x, ib = jb + s;
+  const int r1 = 2 * blockIdx.y * b, r2 = r1 + b;
+  if (r2 >= F.d) return;
+  const int n1 = b, n2 = min(b, F.d - r2);  // r2 < d, so the first block is whole
+  const int per = b / NB;
+  const int ti = blockIdx.x / per, tj = blockIdx.x % per;
+  if (ti * NB >= n2) return;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   float2 sum[4];
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) sum[rr] = make_float2(0.f, 0.f);
-  for (int kb = jb; kb < ib; ++kb) {
+  const int kc0 = stage == 0 ? tj : 0;
+  const int kc1 = stage == 0 ? (n1 + NB - 1) / NB : ti + 1;
+  for (int kc = kc0; kc < kc1; ++kc) {
     float amax = 0.f, bmax = 0.f;
     for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
       const int u = e / NB, v = e % NB;
-      const int ra = ib * NB + u, ca = kb * NB + v;  // C~[ib][kb]
-      const int rb = kb * NB + u, cb = jb * NB + v;  // X[kb][jb]
-      float2 va = (ra < F.d && ca < F.d && ca < ra) ? F.M[(size_t)ra * F.d + ca] : make_float2(0.f, 0.f);
-      float2 vb = (rb < F.d && cb < F.d) ? F.X[(size_t)rb * F.d + cb] : make_float2(0.f, 0.f);
+      const int ia = ti * NB + u, ka = kc * NB + v;  // A[ia][ka]
+      const int kb = kc * NB + u, jb = tj * NB + v;  // B[kb][jb]
+      float2 va = make_float2(0.f, 0.f), vb = make_float2(0.f, 0.f);
+      if (stage == 0) {
+        if (ia < n2 && ka < n1) va = F.M[(size_t)(r2 + ia) * F.d + (r1 + ka)];               // C~21
+        if (kb < n1 && kb >= jb) vb = F.X[(size_t)(r1 + kb) * F.d + (r1 + jb)];              // X11
+      } else {
+        if (ia < n2 && ka <= ia) va = F.X[(size_t)(r2 + ia) * F.d + (r2 + ka)];              // X22
+        if (kb < n2 && jb < n1) vb = F.X[(size_t)(r1 + jb) * F.d + (r2 + kb)];               // T (transposed)
+      }
       sA[u][v] = va;
       sB[u][v] = vb;
       amax = fmaxf(amax, fabsf(va.x));
@@ -252,28 +264,14 @@ __global__ void __launch_bounds__(256) inv_offdiag_kernel(FParams F, int s) {
     for (int rr = 0; rr < 4; ++rr) sum[rr] = df_add(sum[rr], acc[rr].value(sigma));
     __syncthreads();
   }
-  // X[ib][jb] = -X[ib][ib] * S
-#pragma unroll
-  for (int rr = 0; rr < 4; ++rr) sS[ty + 8 * rr][tx] = sum[rr];
-  for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
-    const int u = e / NB, v = e % NB;
-    const int ra = ib * NB + u, ca = ib * NB + v;
-    sA[u][v] = (ra < F.d && ca < F.d) ? F.X[(size_t)ra * F.d + ca] : make_float2(0.f, 0.f);
-  }
-  __syncthreads();
-  float2 out[4];
-#pragma unroll
-  for (int rr = 0; rr < 4; ++rr) out[rr] = make_float2(0.f, 0.f);
-  for (int t = 0; t < NB; ++t) {
-    const float2 bv = sS[t][tx];
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) out[rr] = df_add(out[rr], df_mul(sA[ty + 8 * rr][t], bv));
-  }
-  const int gc = jb * NB + tx;
+  const int j = tj * NB + tx;
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
-    const int gr = ib * NB + ty + 8 * rr;
-    if (gr < F.d && gc < F.d) F.X[(size_t)gr * F.d + gc] = df_neg(out[rr]);
+    const int i = ti * NB + ty + 8 * rr;
+    if (i < n2 && j < n1) {
+      if (stage == 0) F.X[(size_t)(r1 + j) * F.d + (r2 + i)] = sum[rr];
+      else F.X[(size_t)(r2 + i) * F.d + (r1 + j)] = df_neg(sum[rr]);
+    }
   }
 }
 
@@ -322,13 +320,16 @@ cudaError_t factor_launch(const float* H, int d, float* Lhat, void* ws, int32_t*
     diag_factor_kernel<<<1, dim3(NB, NB), 0, stream>>>(F, kb);
     const int rows = d - std::min(d, (kb + 1) * NB);
     if (rows > 0) {
-      panel_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(F, kb);
+      panel_kernel<<<(rows + kPanelRows - 1) / kPanelRows, kPanelRows * NB, 0, stream>>>(F, kb);
       const int nr = F.nb - kb - 1;
       trailing_kernel<<<nr * (nr + 1) / 2, 256, 0, stream>>>(F, kb);
     }
   }
-  inv_diag_kernel<<<F.nb, NB, 0, stream>>>(F);
-  for (int s = 1; s < F.nb; ++s) inv_offdiag_kernel<<<F.nb - s, 256, 0, stream>>>(F, s);
+  for (int b = NB; b < F.d; b *= 2) {
+    const dim3 grid((unsigned)((b / NB) * (b / NB)), (unsigned)((F.d + 2 * b - 1) / (2 * b)));
+    inv_level_kernel<<<grid, 256, 0, stream>>>(F, b, 0);
+    inv_level_kernel<<<grid, 256, 0, stream>>>(F, b, 1);
+  }
   finalize_kernel<<<blocks, 256, 0, stream>>>(F);
   return cudaGetLastError();
 }
