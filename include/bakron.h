@@ -113,7 +113,9 @@ int bakron_prepare(const float* A, const float* B, int64_t m, int64_t n, float* 
  * per-level sum exact in fp32.
  */
 
-/* Workspace bytes bakron_quantize needs for an m x n problem. */
+/* Workspace bytes bakron_quantize needs for an m x n problem: about 72 per
+ * weight, plus, on layers above 2^24 weights, 10 per entry of each factor
+ * (the factors' digits, computed once per solve for the chunk products). */
 size_t bakron_quantize_workspace_size(int64_t m, int64_t n);
 
 /* W: device, m x n; read only.

@@ -117,3 +117,14 @@ def test_roofline_tensor_and_alu_classes():
     assert bench.roofline_for("chunk_push", 1e12, 100.0, {})["peak_basis"].startswith("fallback")
     a = bench.roofline_for("tile_solve", 1e12, 100.0, peaks)
     assert a["bound"] == "alu" and abs(a["peak"] - bench.alu_peak_tflops(2000.0)) < 1e-12
+
+
+def test_antidiagonal_work_count_by_brute_force():
+    """Algorithm 3's multiply-adds with triangular factors: entry (p, q)
+    receives one per earlier entry (i, j), i <= p, j <= q."""
+    import bench
+
+    for m, n in [(1, 1), (2, 3), (5, 4), (7, 9)]:
+        brute = sum(1 for p in range(m) for q in range(n) for i in range(p + 1) for j in range(q + 1)
+                    if (i, j) != (p, q))
+        assert bench.antidiag_macs(m, n) == brute
