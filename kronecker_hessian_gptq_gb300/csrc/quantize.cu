@@ -1167,10 +1167,10 @@ constexpr int kChunkSmem = (int)sizeof(TcSmem<kPacked>);
 
 // Chunk launches of consecutive tile anti-diagonals go round-robin over
 // kChunkStreams streams.  With more than one they overlap and may update
-// the same plane elements, which the fp64 reductions make safe but whose
-// order then varies from run to run; one stream (the default: more were not
-// faster, 19.0 against 19.3 ms on a 4096 x 4096 layer, 95.4 against 91.4 ms
-// on 14336 x 4096) keeps every sum in a fixed order.
+// the same plane elements, which the 64-bit integer reductions keep exact in
+// any order; one stream is the default (more were not faster when measured,
+// with the earlier floating-point reductions: 19.0 against 19.3 ms on a
+// 4096 x 4096 layer, 95.4 against 91.4 ms on 14336 x 4096).
 constexpr int kChunkStreams = 1;
 
 struct StreamSet {
