@@ -35,7 +35,9 @@
 extern "C" {
 #endif
 
-#define BAKRON_ABI_VERSION 1
+/* 2: adds the row-wise, antidiagonal, alphabet, scale, packing, Hessian-factor
+ * and self-test entry points; the entry points of version 1 are unchanged. */
+#define BAKRON_ABI_VERSION 2
 
 typedef enum bakron_status {
   BAKRON_OK = 0,
