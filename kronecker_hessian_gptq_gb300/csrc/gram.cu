@@ -13,8 +13,10 @@
 // operand w_t x_t split into two bf16 terms (hi = bf16(w x), lo = bf16(w x -
 // hi), about 2^-17 relative left over), multiplied in two MMAs.  Each CTA of
 // the Gram kernel then computes one 128 x 128 tile of the lower block
-// triangle over all N samples: one thread loads each stage with two (three)
-// 1-D bulk copies of 16 KB that complete on the stage's mbarrier, one
+// triangle over all N samples: one thread loads each stage with 1-D bulk
+// copies of 16 KB that complete on the stage's mbarrier (the row operand;
+// the column operand unless the tile is diagonal and unweighted; its low
+// half with weights), one
 // thread issues an MMA of M = N = 128, K = 16 per 16 samples into tensor
 // memory (fp32; every bf16 x bf16 product is exact there), and four warps
 // read the tile out and write it and its mirror.
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 1 && lane == 0) {  // the copy thread: each stage is two (three) bulk copies of 16 KB
+  if (warp == 1 && lane == 0) {  // the copy thread: one to three bulk copies of 16 KB per stage
     const uint32_t bytes = (uint32_t)kGTileBytes * (1u + (copy_b ? 1u : 0u) + (kW ? 1u : 0u));
     const size_t rowa = (size_t)bi * P.nkb, rowb = (size_t)bj * P.nkb;
     for (int z = 0; z < nz; ++z) {
