@@ -8,8 +8,6 @@ import os
 import socket
 from contextlib import redirect_stdout
 
-import pytest
-
 from conftest import ROOT
 
 

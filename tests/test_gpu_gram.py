@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from workloads.activations import from_bf16_bits, make_sample_config, make_samples, to_bf16_bits
+from workloads.activations import make_sample_config, make_samples
 
 pytestmark = pytest.mark.gpu
 
