@@ -396,6 +396,22 @@ def run_gram(args, world, dev):
     }
 
 
+# The pages' own BaKron times for the same layer shapes ("BaKron: Efficient
+# Quantization with Kronecker-Factored Hessians", Sec. 6, Table 3: one RTX
+# PRO 6000, float32; their inputs' Hessians and alphabet are not stated):
+# context beside the measured line, not a target and not vs_baseline.
+PAGES_TABLE3_BAKRON_S = {(1024, 1024): 0.025, (2048, 2048): 0.074, (4096, 4096): 0.288, (8192, 8192): 1.839,
+                         (8192, 2048): 0.335, (2048, 8192): 0.322, (14336, 4096): 1.600, (4096, 14336): 1.717}
+
+
+def pages_same_shape(m: int, n: int, ms_per_step: float):
+    """The pages' BaKron time for an m x n layer, if Table 3 lists that shape."""
+    t = PAGES_TABLE3_BAKRON_S.get((m, n))
+    if t is None:
+        return None
+    return {"seconds": t, "hardware": "RTX PRO 6000, float32 (Table 3)", "ratio_pages_over_this": t / (ms_per_step * 1e-3)}
+
+
 def antidiag_macs(m: int, n: int) -> int:
     """Multiply-adds of Algorithm 3 with triangular factors: entry (p, q)
     receives one per earlier entry (i, j) with i <= p, j <= q."""
@@ -583,6 +599,7 @@ def run_ours(args, rank, local_rank, world):
         "solve_alg_tflops": f_alg / (total_ms / args.steps * 1e-3) / 1e12,
         # the solve is a chain of m + n - 1 anti-diagonal steps; on small layers the chain sets the time
         "us_per_antidiagonal_step": total_ms / args.steps * 1e3 / (m + n - 1),
+        "pages_same_shape": pages_same_shape(m, n, total_ms / args.steps),
         "prep_ms": prep_ms,
         "roofline": roof,
         "kernels": kernels,

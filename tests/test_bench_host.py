@@ -126,3 +126,11 @@ def test_antidiagonal_work_count_by_brute_force():
         brute = sum(1 for p in range(m) for q in range(n) for i in range(p + 1) for j in range(q + 1)
                     if (i, j) != (p, q))
         assert bench.antidiag_macs(m, n) == brute
+
+
+def test_pages_same_shape_context():
+    import bench
+
+    c = bench.pages_same_shape(4096, 4096, 16.0)
+    assert c["seconds"] == 0.288 and abs(c["ratio_pages_over_this"] - 18.0) < 1e-9
+    assert bench.pages_same_shape(64, 64, 0.1) is None
