@@ -24,6 +24,14 @@
  *     a non-finite input) are written to a caller-provided device status
  *     word; nothing traps or asserts on the device.
  *   - Return values are bakron_status codes.
+ *   - Process state: the solve keeps, per device, two side streams and a
+ *     pool of ordering events (driver objects, not device memory), created
+ *     by the first call on the device; the no-allocation solve caches its
+ *     scratch array's device address per device.  Both caches remember the
+ *     CUDA context they were made in (cuCtxGetId) and are rebuilt when the
+ *     device's current context changes, e.g. after cudaDeviceReset, so the
+ *     library may be used again after a reset.  Calls from several host
+ *     threads on one device are serialized while they enqueue work.
  */
 #ifndef BAKRON_H_
 #define BAKRON_H_
@@ -36,8 +44,10 @@ extern "C" {
 #endif
 
 /* 2: adds the row-wise, antidiagonal, alphabet, scale, packing, Hessian-factor
- * and self-test entry points; the entry points of version 1 are unchanged. */
-#define BAKRON_ABI_VERSION 2
+ * and self-test entry points; the entry points of version 1 are unchanged.
+ * 3: bakron_quantize_profile reports five kernel classes (the persistent
+ * sweep is class 4); adds bakron_sweep_plan_check. */
+#define BAKRON_ABI_VERSION 3
 
 typedef enum bakron_status {
   BAKRON_OK = 0,
@@ -298,10 +308,14 @@ int bakron_pack_codes(const int32_t* V, int64_t m, int64_t n, int bits, uint8_t*
  * check and set-up (including the factors' block exponents), 1 = tile
  * solve (diagonal blocks and the distance-1 neighbours), 2 = mid pushes
  * (single source tiles), 3 = chunk products (batched source tiles, on the
- * tensor cores).  Synchronizes `stream` before it returns; the
- * events add a little time to every launch.
+ * tensor cores) -- the classes of the launch-per-step schedule -- and 4 =
+ * the persistent sweep, which runs the whole solve (band sweep and every
+ * product) in one cooperative launch; its set-up kernels are not timed.
+ * A solve runs either schedule, so either classes 0..3 or class 4 are
+ * non-zero.  Synchronizes `stream` before it returns; the events add a
+ * little time to every launch.
  */
-#define BAKRON_KERNEL_CLASSES 4
+#define BAKRON_KERNEL_CLASSES 5
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,
@@ -321,6 +335,20 @@ size_t bakron_quantize_host_workspace_size(int64_t m, int64_t n);
 int bakron_quantize_host(const float* W, const float* LA, const float* LB, const float* scales,
                          int bits, int64_t m, int64_t n, int32_t* V, float* Wq, void* dev_ws,
                          size_t dev_ws_bytes, int32_t* status_host, void* stream);
+
+/* Host-only check of the persistent sweep's task plan for an m x n layer
+ * (no GPU involved): every delayed update that the sweep's bands do not
+ * apply themselves -- row terms from source tiles at least 3 tiles back,
+ * column terms from bands at least 2 bands above ("BaKron", App. B eq. (1):
+ * the updates of finished entries are one product L_B E L_A^T restricted
+ * to the later ones) -- is carried by exactly one tensor-core task, and no
+ * task carries one that the bands apply.  stats (host, 3 entries):
+ * [0] number of tasks, [1] the smallest margin in steps, in the ideal
+ * schedule, between a task's sources completing and its first target being
+ * needed, [2] the number of coverage errors.  Returns BAKRON_OK when there
+ * are none, BAKRON_ERR_INVALID_ARG for bad sizes, else 1.
+ */
+int bakron_sweep_plan_check(int64_t m, int64_t n, int64_t* stats);
 
 /* --------------------------------------------------------------- self-test
  * Exercises the device-side timeout path on purpose: one thread waits, with
@@ -348,9 +376,10 @@ int bakron_selftest_wait_timeout(int32_t* status_dev, void* stream);
  * e.g. 1024 x 1024) are rejected with
  * BAKRON_ERR_WORKSPACE before anything is enqueued.
  *
- * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  The call allocates nothing.
+ * The first call on a device (and the first call after the device's context
+ * was replaced, e.g. by cudaDeviceReset) looks up the array's device address
+ * for that device (cudaGetSymbolAddress, with that device current); make
+ * that first call before any stream capture.  The call allocates nothing.
  * Every call on a device shares the one array and leaves its contents
  * behind; each call re-initializes what it reads, but calls that overlap on
  * the GPU (other streams, other host threads) race on it: serialize them.

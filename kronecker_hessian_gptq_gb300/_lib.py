@@ -23,7 +23,7 @@ STATUS_NAMES = {
 DEV_NONFINITE_W = 1
 DEV_BAD_SCALE = 2
 DEV_TIMEOUT = 4
-KERNEL_CLASSES = ("setup", "tile_solve", "mid_push", "chunk_push")
+KERNEL_CLASSES = ("setup", "tile_solve", "mid_push", "chunk_push", "sweep")
 
 _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
@@ -59,6 +59,7 @@ SIGNATURES = {
     "bakron_quantize_host_workspace_size": (_sz, [_i64, _i64]),
     "bakron_quantize_host": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_noalloc": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "bakron_sweep_plan_check": (_int, [_i64, _i64, _vp]),
 }
 
 _lib = None

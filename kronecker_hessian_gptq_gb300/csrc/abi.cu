@@ -4,9 +4,43 @@
 // bakron_status before enqueuing anything; device-side conditions go to the
 // caller's device status words.
 #include <cstdint>
+#include <mutex>
 
 #include "bakron.h"
 #include "internal.h"
+
+namespace bakron {
+
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static cudaError_t lookup = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    lookup = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q);
+    if (lookup == cudaSuccess && q == cudaDriverEntryPointSuccess) get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (lookup == cudaSuccess) lookup = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q);
+    if (lookup == cudaSuccess && q == cudaDriverEntryPointSuccess) get_id = reinterpret_cast<GetId>(f);
+    if (lookup == cudaSuccess && (!get_current || !get_id)) lookup = cudaErrorSymbolNotFound;
+  });
+  if (lookup != cudaSuccess) return lookup;
+  // Make the runtime create or bind the current device's primary context
+  // first (cudaSetDevice initializes it).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return e;
+  void* ctx = nullptr;
+  if (get_current(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+  return get_id(ctx, id) == 0 ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+}  // namespace bakron
 
 namespace {
 
@@ -201,6 +235,11 @@ int bakron_damp(float* G, int64_t d, float rel, void* stream) {
 int bakron_selftest_wait_timeout(int32_t* status_dev, void* stream) {
   if (!status_dev) return BAKRON_ERR_INVALID_ARG;
   return from_cuda(bakron::wait_selftest_launch(status_dev, (cudaStream_t)stream));
+}
+
+int bakron_sweep_plan_check(int64_t m, int64_t n, int64_t* stats) {
+  if (!stats || m < 1 || n < 1 || m * n >= kMaxElems || !bakron::sweep_supported(m, n)) return BAKRON_ERR_INVALID_ARG;
+  return bakron::sweep_plan_check(m, n, stats) == 0 ? BAKRON_OK : 1;
 }
 
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,

@@ -9,11 +9,22 @@ namespace bakron {
 
 constexpr size_t kAlign = 256;
 
+// A process-unique id of the calling thread's current CUDA context (the
+// driver's cuCtxGetId, reached through the runtime's driver entry point, so
+// the library does not link the driver library).  Per-device caches (side
+// streams and events, the no-allocation scratch address) are keyed on it:
+// after cudaDeviceReset the device's next primary context has a new id, and
+// the caches are rebuilt instead of handing out handles or addresses of the
+// destroyed context.
+cudaError_t current_context_id(unsigned long long* id);
+
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Per-kernel-class timing of one solve (diagnostics): CUDA events around
 // every launch, read back after the stream is synchronized.
-constexpr int kKernelClasses = 4;  // 0: input check + offset, 1: tile solve, 2: mid push, 3: chunk push
+// 0: input check + offset, 1: tile solve, 2: mid push, 3: chunk push (the
+// launch-per-step schedule), 4: the persistent sweep (set-up included).
+constexpr int kKernelClasses = 5;
 struct KernelTimer {
   double ms[kKernelClasses];
   int64_t launches[kKernelClasses];
@@ -45,6 +56,16 @@ size_t quantize_workspace_bytes(int64_t m, int64_t n);
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Scales sc,
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
+
+// sweep.cu (the persistent band sweep: one cooperative kernel per solve)
+size_t sweep_workspace_bytes(int64_t m, int64_t n);
+bool sweep_supported(int64_t m, int64_t n);
+// kernel_ms: if given, the call synchronizes and reports the sweep kernel's
+// own time (CUDA events around its launch).
+cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scales sc, Alphabet al, int m, int n,
+                         int32_t* V, float* Wq, void* ws, int32_t* status_dev, cudaStream_t stream,
+                         float* kernel_ms);
+int sweep_plan_check(int64_t m, int64_t n, int64_t* stats);
 
 // antidiag.cu (Algorithm 3, one launch per anti-diagonal; per-row scales)
 size_t antidiag_workspace_bytes(int64_t m, int64_t n);

@@ -22,26 +22,36 @@ static_assert(BAKRON_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size keeps 256-b
 static __device__ __align__(256) unsigned char g_noalloc_scratch[BAKRON_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 128;
-void* g_scratch_address[kMaxDevices];  // device address of the array, per device ordinal
+struct ScratchAddress {
+  void* ptr = nullptr;              // device address of the array
+  unsigned long long ctx_id = 0;    // context it belongs to (0: none yet)
+};
+ScratchAddress g_scratch_address[kMaxDevices];  // per device ordinal
 std::mutex g_scratch_mutex;
 
 // Device address of the array on the current device.  The name
 // g_noalloc_scratch in host code is only a host-side stand-in for the symbol,
 // so the real address is asked from the runtime once per device, with that
-// device current, and cached.
+// device current, and cached together with the id of the context it belongs
+// to; a new context on the device (after cudaDeviceReset) looks it up again.
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  e = bakron::current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_address[dev] == nullptr) {
+  ScratchAddress& a = g_scratch_address[dev];
+  if (a.ptr == nullptr || a.ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_address[dev] = p;
+    a.ptr = p;
+    a.ctx_id = ctx;
   }
-  *out = g_scratch_address[dev];
+  *out = a.ptr;
   return cudaSuccess;
 }
 

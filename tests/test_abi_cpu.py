@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.bakron_abi_version() == 2
+    assert lib.bakron_abi_version() == 3
     assert lib.bakron_status_string(0) == b"BAKRON_OK"
     assert lib.bakron_status_string(4) == b"BAKRON_ERR_WORKSPACE"
     assert lib.bakron_status_string(99) == b"BAKRON_ERR_UNKNOWN"

@@ -94,8 +94,8 @@ def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profiled_traffic("chunk_push", "c3") is None  # no summary
     digest = bench.kernel_source_digest()
-    (tmp_path / "profiles" / "chunk_push_c3_dram.md").write_text(
-        f"# summary\ntraffic_bytes_per_launch: 123456\nsource_sha256: {digest}\n")
+    (tmp_path / "profiles" / "chunk_push_c3_dram.json").write_text(
+        json.dumps({"traffic_bytes_per_launch": 123456, "source_sha256": digest}))
     assert bench.profiled_traffic("chunk_push", "c3") == 123456
     with open(tmp_path / bench.KERNEL_SOURCES[0], "a") as f:
         f.write("\n// a comment edited\n/* and\n another */\n")

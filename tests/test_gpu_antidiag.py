@@ -9,13 +9,13 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tolerances import distortion_tolerance
 from workloads import make_config, random_problem
 
 pytestmark = pytest.mark.gpu
 
 V_MATCH = 0.9999
 D_REL = 1e-4
-D_ABS = 1e-12
 
 
 @pytest.fixture(scope="module")
@@ -56,7 +56,7 @@ def _check(p, V, Wq, Vb):
     assert O.match_fraction(V, Vb) >= V_MATCH
     d_ref = O.distortion(p.W, Wqo, p.A, p.B)
     d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, p.B)
-    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL)
     s = np.ones(p.m, np.float32) if p.scales is None else p.scales
     assert np.array_equal(Wq, (s[:, None] * V.astype(np.float32)).astype(np.float32))
 

@@ -7,13 +7,13 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tolerances import distortion_tolerance
 from workloads import make_config, random_problem
 
 pytestmark = pytest.mark.gpu
 
 V_MATCH = 0.9999
 D_REL = 1e-4
-D_ABS = 1e-12
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +58,7 @@ def test_gptq_against_rowwise_oracle(bk, m, n, bits):
     I = np.eye(m)
     d_ref = O.distortion(p.W, Wqo, p.A, I)
     d_gpu = O.distortion(p.W, Wq, p.A, I)
-    assert abs(d_gpu - d_ref) <= max(D_REL * abs(d_ref), D_ABS)
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, I, D_REL)
 
 
 def test_gptq_equals_bakron_with_identity_output_factor(bk):

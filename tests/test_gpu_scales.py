@@ -17,13 +17,13 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tolerances import distortion_tolerance
 from workloads import make_config, random_problem
 
 pytestmark = pytest.mark.gpu
 
 V_MATCH = 0.9999
 D_REL = 1e-4
-D_ABS = 1e-12
 G_MATCH = 0.999
 ERR_TIE = 1e-9
 
@@ -168,7 +168,7 @@ def test_quantize_range_against_oracle(bk, m, n, alphabet):
     assert O.match_fraction(V, Vo) >= V_MATCH
     d_ref = O.distortion(p.W, Wqo, p.A, p.B)
     d_gpu = O.distortion(p.W, Wq, p.A, p.B)
-    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL)
     assert np.array_equal(Wq.astype(np.float32), (S[:, None] * V.astype(np.float32)).astype(np.float32))
 
 
@@ -184,7 +184,7 @@ def test_quantize_range_rowwise_against_oracle(bk, alphabet):
     I = np.eye(p.m)
     d_ref = O.distortion(p.W, Wqo, p.A, I)
     d_gpu = O.distortion(p.W, Wq, p.A, I)
-    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, I, D_REL)
 
 
 def test_quantize_range_equals_bits_alphabet(bk):
@@ -276,7 +276,7 @@ def test_quantize_scaled_against_oracle(bk, m, n, group, with_cols, with_lb):
     assert O.match_fraction(V, Vo) >= V_MATCH
     d_ref = O.distortion(p.W, Wqo, p.A, Bm)
     d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, Bm)
-    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, Bm, D_REL)
 
 
 def test_quantize_scaled_defaults_equal_range(bk):
@@ -320,4 +320,4 @@ def test_quantize_scaled_multi_tile_grouped(bk):
     assert O.match_fraction(V, Vo) >= V_MATCH
     d_ref = O.distortion(p.W, Wqo, p.A, p.B)
     d_gpu = O.distortion(p.W, Wq.cpu().numpy().astype(np.float64), p.A, p.B)
-    assert abs(d_gpu - d_ref) <= D_REL * abs(d_ref) + D_ABS
+    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL)

@@ -73,6 +73,28 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(env):
         assert np.array_equal(Vn, Vr) and np.array_equal(Wqn, Wqr.cpu().numpy())
 
 
+@pytest.mark.parametrize("case", ["plain_rounding", "near_the_limit"])
+def test_noalloc_matches_workspace_entry_point_edge_cases(env, case):
+    """bits = 0 without scales (the alphabet Z of the 64 x 64 workload), and a
+    1024 x 1024 layer whose solver state nearly fills the fixed scratch, so
+    that its workspace layout reaches closest to the end of the array."""
+    bk, lib, torch = env
+    if case == "plain_rounding":
+        p = random_problem(64, 64, bits=0, seed=21)
+        assert p.scales is None
+    else:
+        p = random_problem(1024, 1024, bits=4, seed=22, w_std=0.02)
+        assert SCRATCH_BYTES // 2 < bk.quantize_workspace_size(1024, 1024) <= SCRATCH_BYTES
+    W, LA, LB, s = _inputs(torch, p)
+    for _ in range(2):
+        Vr, Wqr, str_ = bk.quantize(W, LA, LB, s, p.bits)
+        torch.cuda.synchronize()
+        assert int(str_.item()) == 0
+        rc, Vn, Wqn, st = _noalloc(lib, torch, W, LA, LB, s, p.bits)
+        assert rc == 0 and st == 0, (rc, st)
+        assert np.array_equal(Vn, Vr.cpu().numpy()) and np.array_equal(Wqn, Wqr.cpu().numpy())
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(env):
     bk, lib, torch = env
     m, n = 2048, 2048  # 288 MiB of solver state
