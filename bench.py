@@ -49,8 +49,16 @@ def alu_peak_tflops(sm_max_mhz: float) -> float:
 
 # Kernel classes on the tensor cores, with the bf16 multiply-adds their exact
 # digit split performs per algorithmic multiply-add (5 factor digits x 6
-# source digits, the 20 pairs of levels 0..5).
-TENSOR_CLASSES = {"chunk_push": 20}
+# source digits, the 20 pairs of levels 0..5).  "sweep" is the persistent
+# solve kernel, which runs the whole solve (the band sweep on the fp32 pipes
+# and every product on the tensor cores): its entry is the solve's own rate
+# against the tensor roofline of the precision mode, i.e. the measured bf16
+# peak divided by the 20 digit pairs.
+TENSOR_CLASSES = {"chunk_push": 20, "sweep": 20}
+# Kernel launches of one solve on the persistent sweep: input check, offset,
+# two factor exponent and two factor digit kernels, three task-queue
+# kernels, the sweep.
+SWEEP_LAUNCHES = 10
 BF16_FALLBACK_TFLOPS = 1900.0  # used only without a measured peak
 
 
@@ -583,7 +591,10 @@ def run_ours(args, rank, local_rank, world):
     kernels = {name: {"ms": kms[c], "launches": kl[c], "alg_tflops": (kf[c] / (kms[c] * 1e-3) / 1e12) if kms[c] else 0}
                for c, name in enumerate(_lib.KERNEL_CLASSES)}
     dom = max(range(ncls), key=lambda c: kms[c])
-    launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
+    if kl[ncls - 1]:  # the persistent sweep
+        launches_per_step = SWEEP_LAUNCHES
+    else:  # launch-per-step schedule: class 0 is two launches per solve
+        launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
 
     # End to end through the host entry point: pinned host inputs in, codes out.
     Wh = torch.from_numpy(p.W).pin_memory()

@@ -1073,7 +1073,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   // this device can co-schedule its cooperative grid; the launch-per-step
   // tile wavefront below serves the one-sided case (row-wise GPTQ) and
   // devices without cooperative launch.
-  if (false && LB && sweep_supported(m, n)) {
+  if (LB && sweep_supported(m, n)) {
     float ms = 0.f;
     cudaError_t e = sweep_launch(W, LA, LB, sc, al, m, n, V, Wq, ws, status_dev, stream, timer ? &ms : nullptr);
     if (e != cudaErrorCooperativeLaunchTooLarge) {

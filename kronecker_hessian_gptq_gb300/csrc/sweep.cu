@@ -60,23 +60,29 @@ using sweep::Task;
 constexpr int kRingWarps = 8;
 constexpr int kSlots = 12;        // anti-diagonals held per ring lane: k0, k0 + 8, ..., k0 + 88
 constexpr int kCSlots = 4;        // of which the first 4 can still receive in-band column terms
-constexpr int kRing = 48;         // columns kept in the shared rings (E, v, Wq, G, band-above sums)
+constexpr int kRing = 40;         // columns kept in the shared rings of rounded values (E, v, Wq, G)
+constexpr int kBag = 48;          // band-above G columns kept in shared memory
+constexpr int kFar = 24;          // anti-diagonals of staged inputs and delayed sums
 constexpr int kWoWarp = 8;        // write-out warp
-constexpr int kBaWarp0 = 9;       // band-above warps 9, 10
-constexpr int kBandWarps = 11;
-constexpr int kEpiWarp0 = 12;     // epilogue warps 12..15 (tensor-memory lane quarters 0..3)
-constexpr int kMmaWarp = 16;
-constexpr int kSchedWarp = 17;
-constexpr int kWarps = 18;
+constexpr int kLoadWarp = 9;      // loader warp: inputs, delayed sums and the band above's G, staged ahead
+constexpr int kBandWarps = 10;
+constexpr int kEpiWarp0 = 10;     // epilogue warps 10..13; warp w reads tensor-memory lane quarter w % 4
+constexpr int kMmaWarp = 14;
+constexpr int kSchedWarp = 15;
+constexpr int kWarps = 16;        // 4 warps per SM sub-partition: 128 registers each
 constexpr int kThreads = kWarps * 32;
-constexpr int kProdThreads = (kWarps - kEpiWarp0) * 32;  // 192
 constexpr int kTcM = 128;         // target lines per product group
-constexpr int kGroups = sweep::kGroupsPerTask;
 constexpr int kPubBufs = 3;       // step publications kept (see the ring loop)
 constexpr long long kWaitNs = 1000000000ll;  // one second
 
-// Named barriers (0 is __syncthreads).
-constexpr int kBarRing = 1, kBarProd = 2, kBarEpi = 3, kBarBand = 4;
+// Named barriers (0 is __syncthreads).  The ring warps' step barrier
+// alternates between two ids, step s using kBarRing + (s & 1): the warp that
+// rounds step s arrives early at step s + 1's barrier (bar.arrive) and next
+// waits at step s + 2's; with one id that wait could land in step s + 1's
+// phase if it is not complete yet, with two it cannot (passing step s + 1's
+// barrier requires every warp to have passed step s's).
+constexpr int kBarRing = 1, kBarBand = 4;  // ring: ids 1 and 2
+__device__ __forceinline__ int ring_bar(int s) { return kBarRing + (s & 1); }
 
 struct SweepParams {
   const float* W;
@@ -90,10 +96,8 @@ struct SweepParams {
   long long* Xc;         // column-direction delayed sums (fixed point), m x n
   long long* Gc;         // row-direction delayed sums, m x n
   float2* Gt;            // published G: [band][column][32 rows]
-  __nv_bfloat16* DE;     // E digits [digit][row][ldE]
-  __nv_bfloat16* DGt;    // G digits [digit][column][ldG]
-  size_t dstrideE, dstrideG;
-  int ldE, ldG;
+  __nv_bfloat16* EB;     // E digits in source blocks [band][tile][digit][32 rows x 32 columns, core-matrix order]
+  __nv_bfloat16* GB;     // G digits in source blocks [column tile][band][digit][32 columns x 32 rows]
   const signed char* expA;
   const signed char* expB;
   const __nv_bfloat16* FdA;
@@ -114,12 +118,17 @@ struct SweepParams {
 
 // ------------------------------------------------------------- shared memory
 struct ProdSmem {
-  __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs (core-matrix layout, SBO 512 B)
-  __nv_bfloat16 Bd[kDigD * T * CK];         // source digits, digit-major rows x K (SBO = K / 8 * 128 B)
-  int er[kGroups][kTcM];                    // factor row exponents of each group
-  uint64_t afull[2], aempty[2], gfull[2], gempty[2], bfull;
+  struct Buf {
+    __nv_bfloat16 A[kDigF][kTcM * kSlab];  // factor digit slab (core-matrix layout, SBO 512 B)
+    __nv_bfloat16 B[kDigD * T * kSlab];     // source block: 6 digits x 32 lines x 32 (SBO 512 B)
+  } buf[2];
+  int4 gdesc[2];        // group in tensor-memory half h: (task, group, last of task, -)
+  int unit[2];          // unit in buffer p: 1 first slab of its group, 2 last slab, 4 stop
+  uint64_t full[2], empty[2], gfull[2], gempty[2];
+  uint64_t gready[2];   // gdesc[h] written (scheduler lane's arrival, a release the epilogue acquires)
+  uint64_t edone;       // the epilogue threads' updates of a task are fenced (128 arrivals per task)
   uint32_t tmem_base;
-  int task_idx;                             // canonical index of the posted task, -1: stop
+  int pad[3];
 };
 
 struct BandSmem {
@@ -130,15 +139,21 @@ struct BandSmem {
   float2 sG[kPubBufs][T];       // and row transforms
   float4 EV[kRing][T];          // (E hi, E lo, v, Wq) by (column mod kRing, row)
   float2 Gr[kRing][T];          // G by (column mod kRing, row)
-  float2 BA[kRing][T];          // band-above sums by (column mod kRing, row)
-  float2 Ga[2][T];              // band-above staging of one G column per warp
+  float BAh[kBag][T + 1];       // G of band I - 1 by (column mod kBag, row): high words
+  float BAl[kBag][T + 1];       // and low words
+  float2 FC[kFar][T];           // W0 + column-direction delayed sum, by (anti-diagonal mod kFar, row)
+  float2 FR[kFar][T];           // row-direction delayed sum
+  float FS[kFar][T];            // entry scale
   int rounded;                  // last band step rounded
   int written;                  // last band step written out
-  int ba_done[2];               // last column of each band-above warp's sums
+  int bag_done;                 // last band-above column staged
+  int far_done;                 // last anti-diagonal staged
   int panel;                    // last L_A panel loaded
 };
 
 constexpr size_t kSmemBytes = sizeof(ProdSmem) + sizeof(BandSmem) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM: at most 227 KB of shared memory");
+static_assert(sizeof(ProdSmem) % 16 == 0, "the band state after it stays 16-byte aligned");
 
 // ------------------------------------------------------------------ waits
 __device__ __forceinline__ long long gtimer() {
@@ -147,23 +162,25 @@ __device__ __forceinline__ long long gtimer() {
   return t;
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
+__device__ __forceinline__ int ld_relaxed(const int* p) {
   int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned ld_acquire_u(const unsigned* p) {
+__device__ __forceinline__ unsigned ld_relaxed_u(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Acquire fence: every load after it sees the writes released before the
+// relaxed observations made before it.
+__device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ long long ldcg_ll(const long long* p) { return __ldcg(p); }
 
 __device__ __forceinline__ bool aborted(const Header* h) { return *(volatile const int*)&h->abort != 0; }
 
@@ -172,25 +189,12 @@ __device__ __noinline__ void raise_timeout(const SweepParams& P) {
   atomicExch(&P.hdr->abort, 1);
 }
 
-// Spins until *p >= v (global, acquire).  False once the wait ran out or the
-// kernel is aborting: the caller then proceeds as if it had been satisfied.
-__device__ bool wait_global_ge(const SweepParams& P, const int* p, int v) {
-  if (ld_acquire(p) >= v) return true;
+// Spins until *p >= v with relaxed loads; the caller fences before reading
+// what the value guards.  False once the wait ran out or the kernel aborts.
+__device__ bool wait_relaxed_ge(const SweepParams& P, const int* p, int v) {
+  if (ld_relaxed(p) >= v) return true;
   const long long t0 = gtimer();
-  while (ld_acquire(p) < v) {
-    if (aborted(P.hdr)) return false;
-    if (gtimer() - t0 > kWaitNs) {
-      raise_timeout(P);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
-}
-__device__ bool wait_count(const SweepParams& P, const unsigned* p, unsigned v) {
-  if (ld_acquire_u(p) >= v) return true;
-  const long long t0 = gtimer();
-  while (ld_acquire_u(p) < v) {
+  while (ld_relaxed(p) < v) {
     if (aborted(P.hdr)) return false;
     if (gtimer() - t0 > kWaitNs) {
       raise_timeout(P);
@@ -228,6 +232,16 @@ __device__ __forceinline__ float entry_scale(const SweepParams& P, int r, int q)
   if (P.scales) sv = P.scales[(size_t)r * P.ngroups + q / P.group];
   if (P.cscales) sv = __fmul_rn(sv, P.cscales[q]);
   return sv;
+}
+
+// The six bf16 digits of a solver value (put_digits) into a source block:
+// line l, depth k of a 32 x 32 block, digit b at element b * 1024 +
+// (l / 8) * 256 + (k / 8) * 64 + (l % 8) * 8 + k % 8 -- the K-major
+// core-matrix order of the products' B operand (8 x 16-byte core matrices,
+// leading offset 128 B, stride offset 512 B), so that a block is one bulk
+// copy and six stacked digits are one operand.
+__device__ __forceinline__ void put_block_digits(__nv_bfloat16* blk, int l, int k, float2 x, float sc) {
+  put_digits(blk, 1024, (size_t)((l >> 3) * 256 + (k >> 3) * 64 + (l & 7) * 8 + (k & 7)), x, sc);
 }
 
 // ---------------------------------------------------------------- band role
@@ -280,43 +294,26 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
     cL[i] = 0.f;
   }
   int k0 = w;  // next anti-diagonal this warp rounds (slot 0)
-  // Delayed sums, input and scale of the entry of slot 1, loaded ahead.
-  float pW = 0.f, pS = 1.f;
-  long long pX = 0, pG = 0;
   float se0 = 1.f, rcp0 = 1.f;  // scale of slot 0's entry
 
-  auto prefetch = [&](int k) {
-    const int q = k - p;
-    pW = 0.f;
-    pX = pG = 0;
-    pS = 1.f;
-    if (vr && q >= 0 && q < n) {
-      wait_count(P, P.cnt_col + (size_t)I * P.ncs + (q >> 3), P.exp_col[(size_t)I * P.ncs + (q >> 3)]);
-      const size_t ri = ((size_t)I * P.Nt + (q >> 5)) * 4 + (p >> 3);
-      wait_count(P, P.cnt_row + ri, P.exp_row[ri]);
-      const size_t o = (size_t)r * n + q;
-      pW = __ldg(P.W + o);
-      pX = ldcg_ll(P.Xc + o);
-      pG = ldcg_ll(P.Gc + o);
-      pS = entry_scale(P, r, q);
-    }
-  };
-  // Slot 0 now holds anti-diagonal k: add its input, delayed sums and band-above sum.
+  // Slot 0 now holds anti-diagonal k: add its input and delayed sums (staged
+  // by the loader warp) and its band-above sum.
   auto refresh0 = [&](int k) {
     const int q = k - p;
-    if (I > 0) {
-      const int need = min(k, n - 1);
-      wait_shared_ge(P, &sb.ba_done[0], need);
-      wait_shared_ge(P, &sb.ba_done[1], need);
-    }
-    se0 = pS;
-    rcp0 = __frcp_rn(pS);
+    wait_shared_ge(P, &sb.far_done, k);
+    if (I > 0) wait_shared_ge(P, &sb.bag_done, min(k, n - 1));
+    const int f = k % kFar;
+    se0 = sb.FS[f][p];
+    rcp0 = __frcp_rn(se0);
     if (vr && q >= 0 && q < n) {
       OffsetAcc c{cH[0], cL[0]}, rr{rH[0], rL[0]};
-      c.mac(1.f, pW);
-      c.mac(1.f, df_from_fixed(pX, from_units));
-      if (I > 0) c.mac(1.f, sb.BA[q % kRing][p]);
-      rr.mac(1.f, df_from_fixed(pG, from_units));
+      c.mac(1.f, sb.FC[f][p]);
+      if (I > 0) {  // band I - 1: sum_i L_B[r, 32(I-1) + i] G[32(I-1) + i, q]
+        const int slot = q % kBag;
+#pragma unroll 8
+        for (int i = 0; i < T; ++i) c.mac(sb.LB1[p][i], make_float2(sb.BAh[slot][i], sb.BAl[slot][i]));
+      }
+      rr.mac(1.f, sb.FR[f][p]);
       cH[0] = c.H;
       cL[0] = c.L;
       rH[0] = rr.H;
@@ -360,17 +357,14 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
     }
   };
 
-  // Set-up: slot 0 = anti-diagonal w, prefetched and refreshed; slot 1 prefetched.
-  prefetch(k0);
-  refresh0(k0);
-  prefetch(k0 + 8);
+  refresh0(k0);  // slot 0 = anti-diagonal w
   bool arrived = false;  // this warp already arrived at the current step's barrier
 
   for (int s = 0; s < steps; ++s) {
-    if (!arrived) bar_sync(kBarRing, kRingWarps * 32);
+    if (!arrived) bar_sync(ring_bar(s), kRingWarps * 32);
     arrived = false;
     // The source L_A panel of the newest source column s - 1 (row 0's).
-    if (s >= 1 && ((s - 1) & (T - 1)) == 0) wait_shared_ge(P, &sb.panel, (s - 1) >> 5);
+    if (s >= 1 && ((s - 1) & (T - 1)) == 0 && ((s - 1) >> 5) < P.Nt) wait_shared_ge(P, &sb.panel, (s - 1) >> 5);
     if (k0 == s) {
       if (s >= 1) fold(s - 1, 0, 1);
       // Round anti-diagonal s: entry (p, s - p).
@@ -390,7 +384,7 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
         g = df_add(two_sum(rH[0] - sigma, rL[0]), e);
         wq = se0 * v;
       }
-      // The rings' slots of column q were written out at least 16 steps ago.
+      // The rings' slots of column q were written out at least kRing - 32 steps ago.
       wait_shared_ge(P, &sb.written, s - (kRing - T));
       const int buf = s % kPubBufs;
       sb.sE[buf][p] = e;
@@ -402,7 +396,7 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       __syncwarp();
       __threadfence_block();
       if (p == 0) *(volatile int*)&sb.rounded = s;
-      bar_arrive(kBarRing, kRingWarps * 32);
+      bar_arrive(ring_bar(s + 1), kRingWarps * 32);
       arrived = true;
       if (s >= 1) fold(s - 1, 1, kSlots);
       // Shift the ring: slot i takes slot i + 1, a new anti-diagonal enters.
@@ -421,20 +415,18 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       cH[kCSlots - 1] = sigma;
       cL[kCSlots - 1] = 0.f;
       k0 += 8;
-      if (k0 < steps) {
-        refresh0(k0);
-        prefetch(k0 + 8);
-      }
+      if (k0 < steps) refresh0(k0);
     } else if (s >= 1) {
       fold(s - 1, 0, kSlots);
     }
   }
-  if (!arrived) bar_sync(kBarRing, kRingWarps * 32);
+  if (!arrived) bar_sync(ring_bar(steps), kRingWarps * 32);
 }
 
 // The write-out warp of band I: V, Wq and the digits of E for every row
 // tile a row completes, G (published and as digits) for every column the
 // band completes, the L_A panels ahead of the sweep, and the band's progress.
+// Every decision of this warp is taken by lane 0 and broadcast.
 __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float sigma) {
   const int lane = threadIdx.x & 31;
   const int n = P.n, steps = n + T - 1;
@@ -455,7 +447,18 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
       if (lane == 0) *(volatile int*)&sb.panel = next_panel;
       ++next_panel;
     }
-    wait_shared_ge(P, &sb.rounded, s);
+    {  // wait for step s to be rounded
+      const long long t0 = gtimer();
+      for (;;) {
+        int go = 0;  // 1: step s is rounded (or the kernel is aborting), 2: the wait ran out
+        if (lane == 0)
+          go = (*(volatile int*)&sb.rounded >= s || aborted(P.hdr)) ? 1 : (gtimer() - t0 > kWaitNs ? 2 : 0);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (go == 2 && lane == 0) raise_timeout(P);
+        if (go) break;
+        __nanosleep(20);
+      }
+    }
     // Row tiles completed at step s: row p completes tile j when it rounds
     // column min(32j + 31, n - 1).
     for (int ev = 0; ev < 2; ++ev) {
@@ -471,81 +474,170 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
       }
       if (p < 0 || r0 + p >= P.m) continue;
       const int q = T * j + lane;
+      float2 e = make_float2(0.f, 0.f);  // past the last column: zero digits (the products' K padding)
       if (q < n) {
         const float4 ev4 = sb.EV[q % kRing][p];
         const size_t o = (size_t)(r0 + p) * n + q;
         P.V[o] = (int32_t)ev4.z;
         P.Wq[o] = ev4.w;
-        put_digits(P.DE, P.dstrideE, (size_t)(r0 + p) * P.ldE + q, make_float2(ev4.x, ev4.y), dsc);
+        e = make_float2(ev4.x, ev4.y);
       }
+      put_block_digits(P.EB + ((size_t)I * P.Nt + j) * (kDigD * 1024), p, lane, e, dsc);
     }
     // The column completed at step s (row 31 rounded it).
     const int c = s - (T - 1);
     if (c >= 0 && c < n) {
-      const float2 g = sb.Gr[c % kRing][lane];
+      const float2 g = sb.Gr[c % kRing][lane];  // zero for rows past the last (the products' K padding)
       P.Gt[((size_t)I * n + c) * T + lane] = g;
-      if (r0 + lane < P.m) put_digits(P.DGt, P.dstrideG, (size_t)c * P.ldG + r0 + lane, g, dsc);
+      put_block_digits(P.GB + ((size_t)(c / T) * P.Mt + I) * (kDigD * 1024), c % T, lane, g, dsc);
     }
     __syncwarp();
     if (lane == 0) *(volatile int*)&sb.written = s;
+    // Publish: the warp's stores happen before lane 0's release (warp
+    // barrier), and the release makes them visible with the new progress.
     if ((s & 3) == 3 || s == steps - 1) {
-      __threadfence();
-      __syncwarp();
       if (lane == 0) st_release(P.progress + I, s);
     }
   }
 }
 
-// Band-above warp h (0, 1) of band I: for columns c = h (mod 2), the sums
-// sum_i L_B[32I + p, 32(I-1) + i] G[32(I-1) + i, c] of band I - 1's
-// published G, into the ring BA.
-__device__ void band_above(const SweepParams& P, BandSmem& sb, int I, int h, float sigma) {
-  const int lane = threadIdx.x & 31;
-  const int n = P.n;
-  if (I == 0) {
-    if (lane == 0) *(volatile int*)&sb.ba_done[h] = n;
-    return;
-  }
-  int seen = -1;  // band I - 1's progress, last read
-  for (int c = h; c < n; c += 2) {
-    if (seen < c + T - 1) {
-      wait_global_ge(P, P.progress + (I - 1), c + T - 1);
-      seen = ld_acquire(P.progress + (I - 1));
+// The loader warp of band I, running ahead of the ring warps:
+//  * band-above G: column c of band I - 1 goes to slot c mod kBag once band
+//    I - 1 has written it out (its step c + 31) and the slot's previous
+//    column (c - kBag) is consumed -- row p folds column c' at the refresh
+//    of anti-diagonal c' + p, done by the warp that rounds c' + p - 8 before
+//    its barrier of step c' + p - 6, so all rows did once step c' + 25 is
+//    rounded;
+//  * for anti-diagonal k (entries (p, k - p)), once every product serving
+//    those entries has counted its completion: W0 plus the column-direction
+//    delayed sum, the row-direction delayed sum and the entry scale, to slot
+//    k mod kFar.  The ring refreshes anti-diagonal k (during step k - 8);
+//    the slot's previous anti-diagonal (k - kFar) is consumed once step
+//    k - kFar - 5 is rounded.  The loader stays at most 24 anti-diagonals
+//    ahead of the ring.
+// Counters and progress are polled with relaxed loads, a batch at a time,
+// followed by one acquire fence before the data they guard is read.
+// Every decision of this warp is taken by lane 0 or by a warp vote.
+constexpr int kLoadBatch = 8;
+
+__device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sigma) {
+  const int lane = threadIdx.x & 31, p = lane;
+  const int n = P.n, steps = n + T - 1;
+  const int r = I * T + p;
+  const bool vr = r < P.m;
+  const float from_units = pow2f(fixed_unit_exp(sigma));
+  int next_bag = I > 0 ? 0 : n, seen = -1;
+  int next_k = 0;
+  long long idle_since = gtimer();
+  while (next_k < steps || next_bag < n) {
+    int rd = 0;
+    if (lane == 0) rd = *(volatile int*)&sb.rounded;
+    const int rounded = __shfl_sync(0xffffffffu, rd, 0);
+    bool did = false;
+    // Band-above columns.
+    if (next_bag < n && next_bag - kBag + 25 <= rounded) {
+      if (seen < next_bag + T - 1) {
+        int pr = 0;
+        if (lane == 0) pr = ld_relaxed(P.progress + (I - 1));
+        const int now = __shfl_sync(0xffffffffu, pr, 0);
+        if (now > seen) {
+          fence_acquire();
+          seen = now;
+        }
+      }
+      int c1 = next_bag;
+      while (c1 < n && c1 - kBag + 25 <= rounded && c1 + T - 1 <= seen) ++c1;
+      for (int c = next_bag; c < c1; ++c) {
+        const float2 g = __ldcg(P.Gt + ((size_t)(I - 1) * n + c) * T + lane);
+        sb.BAh[c % kBag][lane] = g.x;
+        sb.BAl[c % kBag][lane] = g.y;
+      }
+      if (c1 > next_bag) {
+        __syncwarp();
+        __threadfence_block();
+        if (lane == 0) *(volatile int*)&sb.bag_done = c1 - 1;
+        next_bag = c1;
+        did = true;
+      }
     }
-    // The ring slot of column c - kRing is free once every row consumed it:
-    // row p consumes column c' at the refresh of anti-diagonal c' + p, done
-    // by the warp that rounds c' + p - 8 before its barrier of step
-    // c' + p - 6; so step c' + 31 - 6 rounded means all rows did.
-    wait_shared_ge(P, &sb.rounded, c - kRing + T - 6);
-    sb.Ga[h][lane] = __ldcg(P.Gt + ((size_t)(I - 1) * n + c) * T + lane);
-    __syncwarp();
-    OffsetAcc a;
-    a.init(sigma);
-#pragma unroll 8
-    for (int i = 0; i < T; ++i) a.mac(sb.LB1[lane][i], sb.Ga[h][i]);
-    sb.BA[c % kRing][lane] = a.value(sigma);
-    __syncwarp();
-    __threadfence_block();
-    if (lane == 0) *(volatile int*)&sb.ba_done[h] = c;
+    // Inputs and delayed sums of the next batch of anti-diagonals.
+    const int kend = min(min(steps, next_k + kLoadBatch), rounded + 25);
+    if (next_k < kend) {
+      // Poll this lane's counters for the batch (relaxed), all lanes until ready.
+      bool ready = true;
+      for (int k = next_k; k < kend && ready; ++k) {
+        const int q = k - p;
+        if (vr && q >= 0 && q < n) {
+          const size_t ci = (size_t)I * P.ncs + (q >> 3);
+          const size_t ri = ((size_t)I * P.Nt + (q >> 5)) * 4 + (p >> 3);
+          ready = ld_relaxed_u(P.cnt_col + ci) >= P.exp_col[ci] && ld_relaxed_u(P.cnt_row + ri) >= P.exp_row[ri];
+        }
+      }
+      int ab = 0;
+      if (lane == 0) ab = aborted(P.hdr) ? 1 : 0;
+      ab = __shfl_sync(0xffffffffu, ab, 0);
+      if (__all_sync(0xffffffffu, ready) || ab) {
+        fence_acquire();
+        for (int k = next_k; k < kend; ++k) {
+          const int q = k - p, f = k % kFar;
+          float2 cf = make_float2(0.f, 0.f), rf = cf;
+          float sc = 1.f;
+          if (vr && q >= 0 && q < n) {
+            const size_t o = (size_t)r * n + q;
+            cf = df_add(make_float2(__ldg(P.W + o), 0.f), df_from_fixed(__ldcg(P.Xc + o), from_units));
+            rf = df_from_fixed(__ldcg(P.Gc + o), from_units);
+            sc = entry_scale(P, r, q);
+          }
+          sb.FC[f][p] = cf;
+          sb.FR[f][p] = rf;
+          sb.FS[f][p] = sc;
+        }
+        __syncwarp();
+        __threadfence_block();
+        if (lane == 0) *(volatile int*)&sb.far_done = kend - 1;
+        next_k = kend;
+        did = true;
+      }
+    }
+    if (did) {
+      idle_since = gtimer();
+    } else {
+      int out = 0;
+      if (lane == 0) out = (aborted(P.hdr) || gtimer() - idle_since > kWaitNs) ? 1 : 0;
+      out = __shfl_sync(0xffffffffu, out, 0);
+      if (out) {  // nothing could be staged for a second: give up (or the kernel is aborting)
+        if (lane == 0 && !aborted(P.hdr)) raise_timeout(P);
+        if (lane == 0) {
+          *(volatile int*)&sb.bag_done = n;
+          *(volatile int*)&sb.far_done = steps;
+        }
+        break;
+      }
+      __nanosleep(64);
+    }
   }
-  if (lane == 0) *(volatile int*)&sb.ba_done[h] = n;
 }
 
 // --------------------------------------------------------------- product role
-// One task at a time: the scheduler lane fetches the next task of the queue
-// and waits until its sources are complete; the epilogue warps copy the
-// source digits; the scheduler lane streams the factor digit slabs (bulk
-// copies); the MMA lane multiplies (tcgen05, five products per 16-deep
-// step: factor digit a against all source digits stacked along N); the
-// epilogue warps fold the levels into the fixed-point planes and count the
-// task's completion for each of its targets.
+// A stream of slab units through two shared-memory buffers, three roles:
+//  * the scheduler lane fetches tasks in queue order, waits until each
+//    one's sources are complete, and for every (group, slab) of the task
+//    bulk-copies the factor digit slab (A: 128 target lines x 32, five
+//    digits) and the source block (B: 32 lines x 32, six digits, already in
+//    the core-matrix layout) into a free buffer;
+//  * the MMA lane multiplies each unit into the group's tensor-memory half
+//    (five products per 16-deep step: factor digit a against source digits
+//    0 .. 5-a stacked along N, landing on levels a + b);
+//  * the epilogue warps turn each finished group's six levels into
+//    fixed-point updates of the planes, and after a task's last group count
+//    its completion for each of its targets.
+// Units of consecutive tasks follow each other without a pause; mbarriers
+// carry every hand-off, and every wait is bounded.
 struct TaskView {
   Task t;
-  bool row;      // row-direction task (factor L_A, plane Gc) or column-direction (L_B, Xc)
-  bool chunk;    // K up to 128 and 32 source lines, else a slice: K = 32, 8 lines
-  int nl;        // source lines per digit block in Bd (32; a slice uses its first 8)
-  int kmax;      // K extent of Bd (32 or 128)
-  int nslab;     // factor slabs per group
+  bool row;      // row-direction task (factor L_A, sources E, plane Gc) or column-direction (L_B, G, Xc)
+  int lb;        // first of the task's source lines within the 32-line source block
+  int nslab;     // slabs per group (source tiles or bands along K)
   int ngroups;
   int c;         // factor chunk of the source K range
   int s0;        // first slab within the chunk
@@ -557,12 +649,7 @@ __device__ __forceinline__ TaskView view_of(const SweepParams& P, long long idx)
   TaskView v;
   v.t = sweep::decode(P.geom, idx);
   v.row = v.t.type == sweep::kRowSlice || v.t.type == sweep::kRowChunk;
-  v.chunk = v.t.type == sweep::kRowChunk || v.t.type == sweep::kColChunk;
-  // Every product uses the chunk products' tensor-memory layout: source
-  // digit blocks of 32 lines (a slice's 8 lines zero-padded), level l of
-  // the digit products at tensor-memory columns 32 l .. 32 l + 31.
-  v.nl = T;
-  v.kmax = v.chunk ? CK : T;
+  v.lb = v.t.line0 % T;
   v.nslab = (v.t.kLen + kSlab - 1) / kSlab;
   const int dlim = v.row ? P.n : P.m;
   v.tgt0 = T * v.t.t0;
@@ -573,207 +660,214 @@ __device__ __forceinline__ TaskView view_of(const SweepParams& P, long long idx)
   return v;
 }
 
+// Source block of slab sl of a task: row tasks the E digits of (band, source
+// tile), column tasks the G digits of (column tile, source band); 6 digits x
+// 2 KB, contiguous.
+__device__ __forceinline__ const __nv_bfloat16* source_block(const SweepParams& P, const TaskView& v, int sl) {
+  const int k_tile = v.t.k0 / T + sl;
+  const size_t blk = v.row ? ((size_t)v.t.a * P.Nt + k_tile) : ((size_t)(v.t.line0 / T) * P.Mt + k_tile);
+  return (v.row ? P.EB : P.GB) + blk * (kDigD * 1024);
+}
+
 __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool is_epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;
-  const int eD = bound_exp(sigma);
-  const int fexp_unit = fixed_unit_exp(sigma);
-  const uint32_t tmem = sm.tmem_base;
   bool broken = false;
-  // Running counts for the mbarrier phases (all roles count the same way).
-  uint32_t zc = 0;   // factor slabs issued
-  uint32_t gc = 0;   // groups multiplied
-  uint32_t tc = 0;   // tasks whose source digits were loaded
 
-  for (;;) {
-    // Fetch and wait (scheduler lane), post to the product warps.
-    if (warp == kSchedWarp && lane == 0) {
-      int post = -1;
-      if (!aborted(P.hdr)) {
-        const unsigned i = atomicAdd(&P.hdr->queue_head, 1u);
-        if (i < *P.ntasks) {
-          post = P.tasks[i];
-          const Task t = sweep::decode(P.geom, post);
-          for (int b = t.srcBand0; b < t.srcBand1; ++b) wait_global_ge(P, P.progress + b, t.readyStep);
+  if (warp == kSchedWarp) {
+    if (lane == 0) {
+      uint32_t zz = 0, gg = 0;  // slab units and groups issued
+      for (;;) {
+        int idx = -1;
+        if (!aborted(P.hdr) && !broken) {
+          const unsigned i = atomicAdd(&P.hdr->queue_head, 1u);
+          if (i < *P.ntasks) idx = P.tasks[i];
         }
-      }
-      sm.task_idx = post;
-    }
-    bar_sync(kBarProd, kProdThreads);
-    const int idx = sm.task_idx;
-    if (idx < 0) break;
-    const TaskView v = view_of(P, idx);
-    const __nv_bfloat16* Fd = v.row ? P.FdA : P.FdB;
-    const signed char* fexp = v.row ? P.expA : P.expB;
-    const int nch = v.row ? P.nchA : P.nchB;
-    const int nt = v.row ? P.ntA : P.ntB;
-    const int dlim = v.row ? P.n : P.m;
-    const int nz = v.ngroups * v.nslab;
-
-    if (is_epi) {
-      // Source digits: row tasks read E digits of rows line0.. at columns
-      // k0.., column tasks G digits of columns line0.. at rows k0...
-      const int et = tid - kEpiWarp0 * 32;
-      const __nv_bfloat16* dp = v.row ? P.DE : P.DGt;
-      const size_t pst = v.row ? P.dstrideE : P.dstrideG;
-      const int ld = v.row ? P.ldE : P.ldG;
-      const int sbo = v.kmax / 8 * 128;
-      const int pieces = kDigD * v.nl * (v.kmax / 8);
-      for (int e = et; e < pieces; e += 128) {
-        const int k8 = 8 * (e % (v.kmax / 8));
-        const int line = (e / (v.kmax / 8)) % v.nl;
-        const int b = e / (v.kmax / 8 * v.nl);
-        const bool ok = line < v.t.nLines && k8 < v.t.kLen;
-        const __nv_bfloat16* src = dp + (ok ? b * pst + (size_t)(v.t.line0 + line) * ld + v.t.k0 + k8 : 0);
-        const int row = b * v.nl + line;
-        unsigned char* dst = reinterpret_cast<unsigned char*>(sm.Bd) + (row / 8) * sbo + (k8 / 8) * 128 + (row % 8) * 16;
-        cp_async(dst, src, ok ? 16 : 0, 16);
-      }
-      cp_async_commit();
-      for (int e = et; e < v.ngroups * kTcM; e += 128) {
-        const int gi = e / kTcM, rr = e % kTcM;
-        const int gr = v.tgt0 + gi * kTcM + rr;
-        sm.er[gi][rr] = gr < dlim ? (int)fexp[(size_t)gr * nch + v.c] : -100;
-      }
-      cp_async_wait_all();
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.bfull)) : "memory");
-    }
-    bar_sync(kBarProd, kProdThreads);  // er[] written, Bd in flight to the tensor cores' view
-
-    if (warp == kSchedWarp) {
-      if (lane == 0) {
-        for (int z = 0; z < nz; ++z) {
-          const uint32_t zz = zc + z;
-          const int pb = zz & 1, gi = z / v.nslab, s = v.s0 + z % v.nslab;
-          const int t0 = (v.tgt0 + gi * kTcM) / T;
-          const int ntg = min(kTcM / T, nt - t0);
-          const uint32_t bytes = (uint32_t)ntg * 2048u;
-          if (zz >= 2) mbar_wait(&sm.aempty[pb], ((zz >> 1) - 1) & 1u, broken);
-          if (broken) break;
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.afull[pb])),
-                       "r"(bytes * kDigF)
-                       : "memory");
-          const size_t cs = (size_t)v.c * (CK / kSlab) + s;
-#pragma unroll
-          for (int a = 0; a < kDigF; ++a) {
-            const unsigned char* src = reinterpret_cast<const unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t0) * 2048;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                    smem_u32(sm.A[pb][a])),
-                "l"(src), "r"(bytes), "r"(smem_u32(&sm.afull[pb]))
-                : "memory");
-          }
+        if (idx >= 0) {
+          const Task t = sweep::decode(P.geom, idx);
+          for (int b = t.srcBand0; b < t.srcBand1; ++b) wait_relaxed_ge(P, P.progress + b, t.readyStep);
+          // The sources were written by other CTAs' generic stores; the bulk
+          // copies below read them through the async proxy.
+          fence_acquire();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-      }
-      __syncwarp();
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) {
-        mbar_wait(&sm.bfull, tc & 1u, broken);
-        tc_fence_after();
-        const uint32_t sbo = (uint32_t)(v.kmax / 8 * 128);
-        for (int z = 0; z < nz && !broken; ++z) {
-          const uint32_t zz = zc + z;
-          const int pb = zz & 1, gi = z / v.nslab, sl = z % v.nslab;
-          const uint32_t gg = gc + gi, h = gg & 1;
-          if (sl == 0 && gg >= 2) mbar_wait(&sm.gempty[h], ((gg >> 1) - 1) & 1u, broken);
-          mbar_wait(&sm.afull[pb], (zz >> 1) & 1u, broken);
-          if (broken) break;
-          tc_fence_after();
-#pragma unroll
-          for (int j = 0; j < kSlab / 16; ++j) {
-            const uint32_t kb = (uint32_t)((sl * kSlab + 16 * j) / 8) * 128u;
-            const uint64_t db = umma_sdesc(smem_u32(sm.Bd) + kb, 128u, sbo);
+        const int ngroups = idx >= 0 ? view_of(P, idx).ngroups : 1;
+        const TaskView v = view_of(P, idx >= 0 ? idx : 0);
+        const __nv_bfloat16* Fd = v.row ? P.FdA : P.FdB;
+        const int nt = v.row ? P.ntA : P.ntB;
+        for (int gi = 0; gi < ngroups; ++gi) {
+          const uint32_t h = gg & 1;
+          // gdesc[h] and the tensor-memory half h are free once the
+          // epilogue finished group gg - 2.
+          if (gg >= 2) mbar_wait(&sm.gempty[h], ((gg >> 1) - 1) & 1u, broken);
+          sm.gdesc[h] = make_int4(idx, gi, gi == ngroups - 1, 0);
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gready[h])) : "memory");
+          const int nsl = idx >= 0 ? v.nslab : 1;
+          for (int sl = 0; sl < nsl; ++sl) {
+            const uint32_t pb = zz & 1;
+            if (zz >= 2) mbar_wait(&sm.empty[pb], ((zz >> 1) - 1) & 1u, broken);
+            if (idx < 0 || broken) {  // stop: a unit without copies
+              sm.unit[pb] = 4;
+              asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.full[pb])) : "memory");
+              ++zz;
+              break;
+            }
+            sm.unit[pb] = (sl == 0 ? 1 : 0) | (sl == nsl - 1 ? 2 : 0);
+            const int t0 = (v.tgt0 + gi * kTcM) / T;
+            const int ntg = min(kTcM / T, nt - t0);
+            const uint32_t abytes = (uint32_t)ntg * 2048u;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[pb])),
+                         "r"(abytes * kDigF + (uint32_t)(kDigD * 2048))
+                         : "memory");
+            const size_t cs = (size_t)v.c * (CK / kSlab) + v.s0 + sl;
 #pragma unroll
             for (int a = 0; a < kDigF; ++a) {
-              const uint64_t da = umma_sdesc(smem_u32(sm.A[pb][a]) + (uint32_t)(2 * j) * 128u, 128u, 512u);
-              const uint32_t acc = (sl > 0 || j > 0 || a > 0) ? 1u : 0u;
-              umma_bf16(tmem + (uint32_t)(256 * h + 32 * a), da, db, umma_idesc_bf16(kTcM, T * (kDigD - a)), acc);
+              const unsigned char* src =
+                  reinterpret_cast<const unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t0) * 2048;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                      smem_u32(sm.buf[pb].A[a])),
+                  "l"(src), "r"(abytes), "r"(smem_u32(&sm.full[pb]))
+                  : "memory");
+            }
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                    smem_u32(sm.buf[pb].B)),
+                "l"(source_block(P, v, sl)), "r"((uint32_t)(kDigD * 2048)), "r"(smem_u32(&sm.full[pb]))
+                : "memory");
+            ++zz;
+          }
+          ++gg;
+          if (idx < 0 || broken) break;
+        }
+        if (idx < 0 || broken) break;
+      }
+      // Leave no bulk copy in flight: both buffers' last fills have landed
+      // once their full barriers completed (bounded wait).
+      bool gone = false;
+      for (uint32_t pb = 0; pb < 2; ++pb) {
+        const uint32_t uses = (zz + 1 - pb) / 2;
+        if (uses > 0) mbar_wait(&sm.full[pb], (uses - 1) & 1u, gone);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint32_t tmem = sm.tmem_base;
+      uint32_t zz = 0, gg = 0;
+      for (;;) {
+        const uint32_t pb = zz & 1;
+        mbar_wait(&sm.full[pb], (zz >> 1) & 1u, broken);
+        const int f = broken ? 4 : sm.unit[pb];
+        const uint32_t h = gg & 1;
+        if (f & 4) {  // stop: wake the epilogue on the next group's barrier
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gfull[h])) : "memory");
+          break;
+        }
+        if ((f & 1) && gg >= 2) mbar_wait(&sm.gempty[h], ((gg >> 1) - 1) & 1u, broken);
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < kSlab / 16; ++j) {
+          const uint64_t db = umma_sdesc(smem_u32(sm.buf[pb].B) + (uint32_t)(2 * j) * 128u, 128u, 512u);
+#pragma unroll
+          for (int a = 0; a < kDigF; ++a) {
+            const uint64_t da = umma_sdesc(smem_u32(sm.buf[pb].A[a]) + (uint32_t)(2 * j) * 128u, 128u, 512u);
+            const uint32_t acc = ((f & 1) && j == 0 && a == 0) ? 0u : 1u;
+            umma_bf16(tmem + (uint32_t)(256 * h + 32 * a), da, db, umma_idesc_bf16(kTcM, T * (kDigD - a)), acc);
+          }
+        }
+        umma_commit(&sm.empty[pb]);
+        if (f & 2) {
+          umma_commit(&sm.gfull[h]);
+          ++gg;
+        }
+        ++zz;
+      }
+    }
+    __syncwarp();
+  } else {  // epilogue warps
+    const uint32_t tmem = sm.tmem_base;
+    const int qd = warp & 3;          // tensor-memory lane quarter this warp may read
+    const int rr = 32 * qd + lane;    // target line within the group
+    const int eD = bound_exp(sigma);
+    const int fexp_unit = fixed_unit_exp(sigma);
+    uint32_t gg = 0, ntask_done = 0;
+    for (;;) {
+      const uint32_t h = gg & 1;
+      mbar_wait(&sm.gready[h], (gg >> 1) & 1u, broken);
+      mbar_wait(&sm.gfull[h], (gg >> 1) & 1u, broken);
+      const int4 d = sm.gdesc[h];
+      if (d.x < 0 || broken) break;
+      tc_fence_after();
+      const TaskView v = view_of(P, d.x);
+      const int gi = d.y;
+      const int tgt = v.tgt0 + gi * kTcM + rr;  // factor row = target line
+      const bool rok = tgt < v.tgt_end;
+      const signed char* fexp = v.row ? P.expA : P.expB;
+      const int nch = v.row ? P.nchA : P.nchB;
+      const int er = rok ? (int)fexp[(size_t)tgt * nch + v.c] : -100;
+      const int ex = er + eD - 14 - fexp_unit;
+      const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
+      unsigned long long* plane = reinterpret_cast<unsigned long long*>(v.row ? P.Gc : P.Xc);
+      // Row tasks: Gc[source row][target column tgt]; column tasks:
+      // Xc[target row tgt][source column]; source line = line0 + (q - lb).
+      const size_t obase = v.row ? (size_t)v.t.line0 * P.n + tgt : (size_t)tgt * P.n + v.t.line0;
+      const size_t ostep = v.row ? (size_t)P.n : 1;
+#pragma unroll 1
+      for (int qb = v.lb; qb < v.lb + v.t.nLines; qb += 8) {
+        float lv[kLevels][8];
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)
+          tmem_ld(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + T * l + qb), lv[l]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          // levels 0..2 exactly, the rest (below 2^-24 of the total) in one fp32 sum
+          float2 y = two_sum(lv[0][j], lv[1][j] * 0x1p-8f);
+          const float2 y2 = two_sum(y.y, lv[2][j] * 0x1p-16f);
+          const float tail = lv[3][j] * 0x1p-24f + lv[4][j] * 0x1p-32f + lv[5][j] * 0x1p-40f;
+          y = two_sum(y.x, y2.x);
+          y = two_sum(y.x, y.y + (y2.y + tail));
+          const int q = qb - v.lb + j;
+          if (rok && q < v.t.nLines)
+            atomicAdd(plane + obase + (size_t)q * ostep, (unsigned long long)df_to_fixed(y, sc));
+        }
+      }
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gempty[h])) : "memory");
+      if (d.z) {  // the task's last group: every update is in L2; count it per target
+        // All 128 epilogue threads fence their updates, arrive on edone and
+        // wait for its phase (bounded), so that no thread arrives for the
+        // next task before this task's phase is complete.
+        __threadfence();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.edone)) : "memory");
+        mbar_wait(&sm.edone, ntask_done & 1u, broken);
+        if (warp == kEpiWarp0) {  // one warp counts the task's completion
+          if (v.row) {
+            const int nps = v.t.ps1 - v.t.ps0;
+            const int tot = (v.t.t1 - v.t.t0) * nps;
+            for (int e = lane; e < tot; e += 32) {
+              const int t = v.t.t0 + e / nps, ps = v.t.ps0 + e % nps;
+              red_release_add(P.cnt_row + ((size_t)v.t.a * P.Nt + t) * 4 + ps, 1u);
+            }
+          } else {
+            const int ncs = v.t.cs1 - v.t.cs0;
+            const int tot = (v.t.t1 - v.t.t0) * ncs;
+            for (int e = lane; e < tot; e += 32) {
+              const int band = v.t.t0 + e / ncs, cs = v.t.cs0 + e % ncs;
+              red_release_add(P.cnt_col + (size_t)band * P.ncs + cs, 1u);
             }
           }
-          umma_commit(&sm.aempty[pb]);
-          if (sl == v.nslab - 1) umma_commit(&sm.gfull[h]);
         }
+        ++ntask_done;
       }
-      __syncwarp();
-    } else if (is_epi) {
-      const int qd = warp - kEpiWarp0;  // tensor-memory lane quarter
-      const int rr = 32 * qd + lane;    // target line within the group
-      const int lvl_stride = T;
-      for (int gi = 0; gi < v.ngroups; ++gi) {
-        const uint32_t gg = gc + gi, h = gg & 1;
-        mbar_wait(&sm.gfull[h], (gg >> 1) & 1u, broken);
-        tc_fence_after();
-        const int tgt = v.tgt0 + gi * kTcM + rr;  // factor row = target line
-        const bool rok = tgt < v.tgt_end;
-        const int ex = sm.er[gi][rr] + eD - 14 - fexp_unit;
-        const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
-        unsigned long long* plane = reinterpret_cast<unsigned long long*>(v.row ? P.Gc : P.Xc);
-        // Row tasks: Gc[source row line0 + q][target column tgt];
-        // column tasks: Xc[target row tgt][source column line0 + q].
-        const size_t obase = v.row ? (size_t)v.t.line0 * P.n + tgt : (size_t)tgt * P.n + v.t.line0;
-        const size_t ostep = v.row ? (size_t)P.n : 1;
-#pragma unroll 1
-        for (int qb = 0; qb < v.t.nLines; qb += 8) {
-          float lv[kLevels][8];
-#pragma unroll
-          for (int l = 0; l < kLevels; ++l)
-            tmem_ld(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + lvl_stride * l + qb), lv[l]);
-          asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            // levels 0..2 exactly, the rest (below 2^-24 of the total) in one fp32 sum
-            float2 y = two_sum(lv[0][j], lv[1][j] * 0x1p-8f);
-            const float2 y2 = two_sum(y.y, lv[2][j] * 0x1p-16f);
-            const float tail = lv[3][j] * 0x1p-24f + lv[4][j] * 0x1p-32f + lv[5][j] * 0x1p-40f;
-            y = two_sum(y.x, y2.x);
-            y = two_sum(y.x, y.y + (y2.y + tail));
-            if (rok && qb + j < v.t.nLines)
-              atomicAdd(plane + obase + (size_t)(qb + j) * ostep, (unsigned long long)df_to_fixed(y, sc));
-          }
-        }
-        tc_fence_before();
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gempty[h])) : "memory");
-      }
-      // Completion: every update of the task is in L2; count it per target.
-      __threadfence();
-      bar_sync(kBarEpi, 128);
-      if (warp == kEpiWarp0) {
-        if (v.row) {
-          const int nps = (v.t.t1 - v.t.t0) * (v.t.ps1 - v.t.ps0);
-          for (int e = lane; e < nps; e += 32) {
-            const int t = v.t.t0 + e / (v.t.ps1 - v.t.ps0), ps = v.t.ps0 + e % (v.t.ps1 - v.t.ps0);
-            red_release_add(P.cnt_row + ((size_t)v.t.a * P.Nt + t) * 4 + ps, 1u);
-          }
-        } else {
-          const int ncs = v.t.cs1 - v.t.cs0;
-          const int tot = (v.t.t1 - v.t.t0) * ncs;
-          for (int e = lane; e < tot; e += 32) {
-            const int band = v.t.t0 + e / ncs, cs = v.t.cs0 + e % ncs;
-            red_release_add(P.cnt_col + (size_t)band * P.ncs + cs, 1u);
-          }
-        }
-      }
-    }
-    zc += nz;
-    gc += v.ngroups;
-    tc += 1;
-    if (broken) raise_timeout(P);
-    bar_sync(kBarProd, kProdThreads);  // task done: Bd, er and the tensor memory may be reused
-  }
-  // Leave no bulk copy in flight: wait (bounded) for the last phase of both
-  // factor slab buffers the scheduler lane filled.
-  if (warp == kSchedWarp && lane == 0) {
-    bool gone = false;
-    for (int pb = 0; pb < 2; ++pb) {
-      const uint32_t uses = (zc + 1 - pb) / 2;  // fills of buffer pb: slabs zz < zc with zz % 2 == pb
-      if (uses > 0) mbar_wait(&sm.afull[pb], (uses - 1) & 1u, gone);
+      ++gg;
     }
   }
+  if (broken) raise_timeout(P);
 }
 
 // -------------------------------------------------------------------- kernel
-__global__ void __maxnreg__(112) sweep_kernel(SweepParams P) {
+__global__ void __launch_bounds__(kThreads, 1) sweep_kernel(SweepParams P) {
   extern __shared__ __align__(1024) unsigned char sweep_smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sweep_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -785,12 +879,13 @@ __global__ void __maxnreg__(112) sweep_kernel(SweepParams P) {
   if (tid == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.afull[i])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.aempty[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.full[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.gfull[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.gempty[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.gready[i])));
     }
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.bfull)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.edone)));
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == kMmaWarp) {  // two tensor-memory halves of 256 columns
@@ -817,8 +912,8 @@ __global__ void __maxnreg__(112) sweep_kernel(SweepParams P) {
       if (bt == 0) {
         sb.rounded = -1;
         sb.written = -1;
-        sb.ba_done[0] = -1;
-        sb.ba_done[1] = -1;
+        sb.bag_done = I > 0 ? -1 : P.n;
+        sb.far_done = -1;
         sb.panel = 0;
       }
       if (warp == kWoWarp) {
@@ -831,8 +926,8 @@ __global__ void __maxnreg__(112) sweep_kernel(SweepParams P) {
         band_ring(P, sb, I, sigma);
       } else if (warp == kWoWarp) {
         band_writeout(P, sb, I, sigma);
-      } else {
-        band_above(P, sb, I, warp - kBaWarp0, sigma);
+      } else if (warp == kLoadWarp) {
+        band_loader(P, sb, I, sigma);
       }
       bar_sync(kBarBand, kBandWarps * 32);
     }
@@ -954,9 +1049,9 @@ cudaError_t device_info(DeviceInfo& out) {
 
 // ------------------------------------------------------------- workspace
 struct SweepLayout {
-  size_t plane, Gt, DE, DG, dplaneE, dplaneG, expA, expB, FdA, FdB, progress, cnt_col, exp_col, cnt_row, exp_row,
-      buckets, list, ntasks, total;
-  int ldE, ldG, nbuckets;
+  size_t plane, Gt, EB, GB, expA, expB, FdA, FdB, progress, cnt_col, exp_col, cnt_row, exp_row, buckets, list,
+      ntasks, total;
+  int nbuckets;
 };
 
 SweepLayout sweep_layout(int64_t m, int64_t n) {
@@ -969,14 +1064,10 @@ SweepLayout sweep_layout(int64_t m, int64_t n) {
   off += 2 * L.plane;  // Xc, Gc
   L.Gt = off;
   off += align_up((size_t)g.Mt * n * T * sizeof(float2));
-  L.ldE = (int)((n + 7) / 8 * 8);
-  L.ldG = (int)((m + 7) / 8 * 8);
-  L.dplaneE = align_up((size_t)m * L.ldE * sizeof(__nv_bfloat16));
-  L.dplaneG = align_up((size_t)n * L.ldG * sizeof(__nv_bfloat16));
-  L.DE = off;
-  off += kDigD * L.dplaneE;
-  L.DG = off;
-  off += kDigD * L.dplaneG;
+  L.EB = off;
+  off += align_up((size_t)g.Mt * g.Nt * kDigD * 2048);
+  L.GB = off;
+  off += align_up((size_t)g.Nt * g.Mt * kDigD * 2048);
   L.expA = off;
   off += align_up((size_t)n * nchA);
   L.expB = off;
@@ -1038,12 +1129,8 @@ cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scale
   P.Xc = reinterpret_cast<long long*>(base + sizeof(Header));
   P.Gc = reinterpret_cast<long long*>(base + sizeof(Header) + lay.plane);
   P.Gt = reinterpret_cast<float2*>(base + lay.Gt);
-  P.DE = reinterpret_cast<__nv_bfloat16*>(base + lay.DE);
-  P.DGt = reinterpret_cast<__nv_bfloat16*>(base + lay.DG);
-  P.dstrideE = lay.dplaneE / sizeof(__nv_bfloat16);
-  P.dstrideG = lay.dplaneG / sizeof(__nv_bfloat16);
-  P.ldE = lay.ldE;
-  P.ldG = lay.ldG;
+  P.EB = reinterpret_cast<__nv_bfloat16*>(base + lay.EB);
+  P.GB = reinterpret_cast<__nv_bfloat16*>(base + lay.GB);
   P.nchA = (n + CK - 1) / CK;
   P.nchB = (m + CK - 1) / CK;
   P.ntA = P.geom.Nt;
@@ -1070,15 +1157,14 @@ cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scale
   P.hi = al.hi;
 
   // Zeroed state: status, header, the two planes, the counters and buckets;
-  // progress = -1.  Digit rows are padded to 8 entries and the products read
-  // the padding, which must then be zero.
+  // progress = -1.  (The source blocks need no clearing: the write-out warp
+  // writes every entry a product reads along K, zeros past the matrix; lines
+  // past the matrix only feed output columns that are never stored.)
   err = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(P.hdr, 0, sizeof(Header), stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(P.Xc, 0, 2 * lay.plane, stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(base + lay.progress, 0xFF, lay.cnt_col - lay.progress, stream);
   if (err == cudaSuccess) err = cudaMemsetAsync(base + lay.cnt_col, 0, lay.list - lay.cnt_col, stream);
-  if (err == cudaSuccess && (lay.ldE != n || lay.ldG != m))
-    err = cudaMemsetAsync(base + lay.DE, 0, kDigD * (lay.dplaneE + lay.dplaneG), stream);
   if (err != cudaSuccess) return err;
 
   const InputDesc in{W, P.scales, P.cscales, P.ngroups, m, n, P.bounded, P.lo, P.hi, P.hdr, status_dev};

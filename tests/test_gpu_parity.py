@@ -180,3 +180,32 @@ def test_bounded_wait_reports_a_timeout_and_the_context_survives(bk):
     LA, LB = gpu_prepare(bk, p)
     V, Wq = gpu_quantize(bk, p, LA, LB)
     check_against_oracle(p, V, Wq, *O.factors_of(p.A, p.B), "after timeout")
+
+
+def test_two_sided_solves_run_as_the_persistent_sweep(bk):
+    """On a GB300 every two-sided solve is one cooperative sweep launch
+    (profile class 4), not the launch-per-step fallback (classes 0..3), which
+    serves devices that cannot co-schedule the sweep's grid."""
+    import ctypes
+
+    import torch
+
+    from kronecker_hessian_gptq_gb300 import _lib
+
+    lib = bk.load_library()
+    p = random_problem(200, 300, bits=4, seed=12)
+    LA64, LB64 = O.factors_of(p.A, p.B)
+    W, LA, LB, s = _dev(p.W), _dev(LA64), _dev(LB64), _dev(p.scales)
+    ws = torch.empty(bk.quantize_workspace_size(p.m, p.n), dtype=torch.uint8, device="cuda")
+    V = torch.empty((p.m, p.n), dtype=torch.int32, device="cuda")
+    Wq = torch.empty((p.m, p.n), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nc = len(_lib.KERNEL_CLASSES)
+    kms, kl, kf = (ctypes.c_double * nc)(), (ctypes.c_int64 * nc)(), (ctypes.c_double * nc)()
+    rc = lib.bakron_quantize_profile(W.data_ptr(), LA.data_ptr(), LB.data_ptr(), s.data_ptr(), p.bits, p.m, p.n,
+                                     V.data_ptr(), Wq.data_ptr(), ws.data_ptr(), ws.numel(), st.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream, kms, kl, kf)
+    assert rc == 0 and int(st.item()) == 0
+    assert list(kl) == [0, 0, 0, 0, 1], list(kl)
+    assert abs(kf[4] - float(p.m) * p.n * (p.m + p.n)) < 1.0
+    check_against_oracle(p, V.cpu().numpy().astype(np.int64), Wq.cpu().numpy(), LA64, LB64, "sweep profile")
