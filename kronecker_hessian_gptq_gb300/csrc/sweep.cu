@@ -60,9 +60,9 @@ using sweep::Task;
 constexpr int kRingWarps = 8;
 constexpr int kSlots = 12;        // anti-diagonals held per ring lane: k0, k0 + 8, ..., k0 + 88
 constexpr int kCSlots = 4;        // of which the first 4 can still receive in-band column terms
-constexpr int kRing = 40;         // columns kept in the shared rings of rounded values (E, v, Wq, G)
+constexpr int kRing = 44;         // columns kept in the shared rings of rounded values (E, v, Wq, G)
 constexpr int kBag = 48;          // band-above G columns kept in shared memory
-constexpr int kFar = 24;          // anti-diagonals of staged inputs and delayed sums
+constexpr int kFar = 32;          // anti-diagonals of staged inputs and delayed sums
 constexpr int kWoWarp = 8;        // write-out warp
 constexpr int kLoadWarp = 9;      // loader warp: inputs, delayed sums and the band above's G, staged ahead
 constexpr int kBandWarps = 10;
@@ -72,17 +72,23 @@ constexpr int kSchedWarp = 15;
 constexpr int kWarps = 16;        // 4 warps per SM sub-partition: 128 registers each
 constexpr int kThreads = kWarps * 32;
 constexpr int kTcM = 128;         // target lines per product group
-constexpr int kPubBufs = 3;       // step publications kept (see the ring loop)
+constexpr int kPubBufs = 8;       // step publications kept (see the ring barrier)
 constexpr long long kWaitNs = 1000000000ll;  // one second
 
 // Named barriers (0 is __syncthreads).  The ring warps' step barrier
-// alternates between two ids, step s using kBarRing + (s & 1): the warp that
-// rounds step s arrives early at step s + 1's barrier (bar.arrive) and next
-// waits at step s + 2's; with one id that wait could land in step s + 1's
-// phase if it is not complete yet, with two it cannot (passing step s + 1's
-// barrier requires every warp to have passed step s's).
-constexpr int kBarRing = 1, kBarBand = 4;  // ring: ids 1 and 2
-__device__ __forceinline__ int ring_bar(int s) { return kBarRing + (s & 1); }
+// rotates through kRingBars ids, step s using kBarRing + (s mod kRingBars).
+// The warp that rounds step s arrives early at the barriers of steps
+// s + 1 .. s + kRingBars - 1 (bar.arrive) and next waits at step
+// s + kRingBars's: its deferred work (the rest of its fold, the ring shift,
+// the refresh of its next anti-diagonal) then has kRingBars steps instead
+// of one.  A barrier id is reused only kRingBars steps later, and passing a
+// step's barrier requires every warp to have arrived at the step before,
+// so no arrival can land in the wrong phase.  During the steps it skips,
+// the warp reads a step's publication only after the step's rounding is
+// flagged (rounded), and the kPubBufs publication buffers are reused only
+// after every warp has synchronized past the step that read them.
+constexpr int kBarRing = 1, kRingBars = 4, kBarBand = kBarRing + kRingBars;
+__device__ __forceinline__ int ring_bar(int s) { return kBarRing + (s & (kRingBars - 1)); }
 
 struct SweepParams {
   const float* W;
@@ -200,7 +206,7 @@ __device__ bool wait_relaxed_ge(const SweepParams& P, const int* p, int v) {
       raise_timeout(P);
       return false;
     }
-    __nanosleep(64);
+    __nanosleep(128);
   }
   return true;
 }
@@ -323,7 +329,7 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
   // Folds the errors and row transforms published by step ps (anti-diagonal
   // ps) into slots [i0, i1).
   auto fold = [&](int ps, int i0, int i1) {
-    const int buf = ps % kPubBufs;
+    const int buf = ps & (kPubBufs - 1);
     const int qsrc = ps - p;  // this row's source column
     const bool rowok = vr && qsrc >= 0 && qsrc < n;
     const float2 eP = sb.sE[buf][p];
@@ -358,11 +364,14 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
   };
 
   refresh0(k0);  // slot 0 = anti-diagonal w
-  bool arrived = false;  // this warp already arrived at the current step's barrier
+  int skip_until = -1;  // this warp arrived early at the barriers of the steps up to here
 
   for (int s = 0; s < steps; ++s) {
-    if (!arrived) bar_sync(ring_bar(s), kRingWarps * 32);
-    arrived = false;
+    if (s > skip_until) {
+      bar_sync(ring_bar(s), kRingWarps * 32);
+    } else if (s >= 1) {
+      wait_shared_ge(P, &sb.rounded, s - 1);  // step s - 1's publication is written
+    }
     // The source L_A panel of the newest source column s - 1 (row 0's).
     if (s >= 1 && ((s - 1) & (T - 1)) == 0 && ((s - 1) >> 5) < P.Nt) wait_shared_ge(P, &sb.panel, (s - 1) >> 5);
     if (k0 == s) {
@@ -386,7 +395,7 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       }
       // The rings' slots of column q were written out at least kRing - 32 steps ago.
       wait_shared_ge(P, &sb.written, s - (kRing - T));
-      const int buf = s % kPubBufs;
+      const int buf = s & (kPubBufs - 1);
       sb.sE[buf][p] = e;
       sb.sG[buf][p] = g;
       if (q >= 0 && q < n) {
@@ -396,8 +405,8 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       __syncwarp();
       __threadfence_block();
       if (p == 0) *(volatile int*)&sb.rounded = s;
-      bar_arrive(ring_bar(s + 1), kRingWarps * 32);
-      arrived = true;
+      skip_until = min(s + kRingBars - 1, steps - 1);
+      for (int t = s + 1; t <= skip_until; ++t) bar_arrive(ring_bar(t), kRingWarps * 32);
       if (s >= 1) fold(s - 1, 1, kSlots);
       // Shift the ring: slot i takes slot i + 1, a new anti-diagonal enters.
 #pragma unroll
@@ -420,7 +429,6 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       fold(s - 1, 0, kSlots);
     }
   }
-  if (!arrived) bar_sync(ring_bar(steps), kRingWarps * 32);
 }
 
 // The write-out warp of band I: V, Wq and the digits of E for every row
@@ -432,20 +440,24 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
   const int n = P.n, steps = n + T - 1;
   const float dsc = pow2f(7 - bound_exp(sigma));
   const int r0 = I * T;
-  int next_panel = 1;  // panel 0 is loaded before the sweep starts
+  int issued_panel = 0, ready_panel = 0;  // panel 0 is loaded before the sweep starts
   for (int s = 0; s < steps; ++s) {
     // Panel j is first read at step 32j + 1.  Its slot's previous panel
-    // (j - 3) is read for source anti-diagonals up to 32j - 34, the last of
-    // them by a warp's deferred folds before its barrier of step 32j - 31;
-    // this iteration starts once step s - 1 is rounded, so s >= 32j - 24 is
-    // safe, and leaves 25 steps to load.
-    if (next_panel < P.Nt && s >= T * next_panel - 24) {
-      load_panel(P, sb, next_panel);
+    // (j - 3) serves source anti-diagonals up to 32j - 34, read at the
+    // latest by a warp's deferred folds before its barrier of step
+    // 32j - 33 + kRingBars; this iteration starts once step s - 1 is
+    // rounded, so the copy may be issued at s = 32j - 32 + kRingBars and is
+    // waited for at s = 32j - 8.
+    if (issued_panel + 1 < P.Nt && s >= T * (issued_panel + 1) - T + kRingBars) {
+      ++issued_panel;
+      load_panel(P, sb, issued_panel);
+    }
+    if (ready_panel < issued_panel && s >= T * (ready_panel + 1) - 8) {
       cp_async_wait_all();
       __syncwarp();
       __threadfence_block();
-      if (lane == 0) *(volatile int*)&sb.panel = next_panel;
-      ++next_panel;
+      ready_panel = issued_panel;
+      if (lane == 0) *(volatile int*)&sb.panel = ready_panel;
     }
     {  // wait for step s to be rounded
       const long long t0 = gtimer();
@@ -456,7 +468,7 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
         go = __shfl_sync(0xffffffffu, go, 0);
         if (go == 2 && lane == 0) raise_timeout(P);
         if (go) break;
-        __nanosleep(20);
+        __nanosleep(64);
       }
     }
     // Row tiles completed at step s: row p completes tile j when it rounds
@@ -506,19 +518,22 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
 //    I - 1 has written it out (its step c + 31) and the slot's previous
 //    column (c - kBag) is consumed -- row p folds column c' at the refresh
 //    of anti-diagonal c' + p, done by the warp that rounds c' + p - 8 before
-//    its barrier of step c' + p - 6, so all rows did once step c' + 25 is
-//    rounded;
+//    its barrier of step c' + p - 8 + kRingBars, so all rows did once step
+//    c' + 23 + kRingBars is rounded (kBagFree);
 //  * for anti-diagonal k (entries (p, k - p)), once every product serving
 //    those entries has counted its completion: W0 plus the column-direction
 //    delayed sum, the row-direction delayed sum and the entry scale, to slot
-//    k mod kFar.  The ring refreshes anti-diagonal k (during step k - 8);
-//    the slot's previous anti-diagonal (k - kFar) is consumed once step
-//    k - kFar - 5 is rounded.  The loader stays at most 24 anti-diagonals
-//    ahead of the ring.
+//    k mod kFar.  The ring refreshes anti-diagonal k after rounding k - 8,
+//    before its barrier of step k - 8 + kRingBars; so the slot's previous
+//    anti-diagonal (k - kFar) is consumed once step k - kFar - 8 + kRingBars
+//    is rounded.  The loader stays at most kFar anti-diagonals ahead of the
+//    ring, which is enough while kRingBars <= 8.
 // Counters and progress are polled with relaxed loads, a batch at a time,
 // followed by one acquire fence before the data they guard is read.
 // Every decision of this warp is taken by lane 0 or by a warp vote.
+static_assert(kRingBars <= 8, "the loader's staging window assumes refreshes within 8 steps");
 constexpr int kLoadBatch = 8;
+constexpr int kBagFree = T - 1 - 8 + kRingBars;  // steps after column c' until its band-above slot is free
 
 __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sigma) {
   const int lane = threadIdx.x & 31, p = lane;
@@ -534,8 +549,8 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
     if (lane == 0) rd = *(volatile int*)&sb.rounded;
     const int rounded = __shfl_sync(0xffffffffu, rd, 0);
     bool did = false;
-    // Band-above columns.
-    if (next_bag < n && next_bag - kBag + 25 <= rounded) {
+    // Band-above columns: up to kLoadBatch at a time, loads issued together.
+    if (next_bag < n && next_bag - kBag + kBagFree <= rounded) {
       if (seen < next_bag + T - 1) {
         int pr = 0;
         if (lane == 0) pr = ld_relaxed(P.progress + (I - 1));
@@ -546,13 +561,18 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
         }
       }
       int c1 = next_bag;
-      while (c1 < n && c1 - kBag + 25 <= rounded && c1 + T - 1 <= seen) ++c1;
-      for (int c = next_bag; c < c1; ++c) {
-        const float2 g = __ldcg(P.Gt + ((size_t)(I - 1) * n + c) * T + lane);
-        sb.BAh[c % kBag][lane] = g.x;
-        sb.BAl[c % kBag][lane] = g.y;
-      }
+      while (c1 < n && c1 < next_bag + kLoadBatch && c1 - kBag + kBagFree <= rounded && c1 + T - 1 <= seen) ++c1;
       if (c1 > next_bag) {
+        float2 g[kLoadBatch];
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i)
+          if (next_bag + i < c1) g[i] = __ldcg(P.Gt + ((size_t)(I - 1) * n + next_bag + i) * T + lane);
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i)
+          if (next_bag + i < c1) {
+            sb.BAh[(next_bag + i) % kBag][lane] = g[i].x;
+            sb.BAl[(next_bag + i) % kBag][lane] = g[i].y;
+          }
         __syncwarp();
         __threadfence_block();
         if (lane == 0) *(volatile int*)&sb.bag_done = c1 - 1;
@@ -560,37 +580,59 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
         did = true;
       }
     }
-    // Inputs and delayed sums of the next batch of anti-diagonals.
-    const int kend = min(min(steps, next_k + kLoadBatch), rounded + 25);
+    // Inputs and delayed sums of the next batch of anti-diagonals: every
+    // counter of the batch read at once (relaxed), then, when all serving
+    // products have counted, one acquire fence and every data load at once.
+    const int kend = min(min(steps, next_k + kLoadBatch), rounded + kFar + 1);
     if (next_k < kend) {
-      // Poll this lane's counters for the batch (relaxed), all lanes until ready.
       bool ready = true;
-      for (int k = next_k; k < kend && ready; ++k) {
-        const int q = k - p;
-        if (vr && q >= 0 && q < n) {
-          const size_t ci = (size_t)I * P.ncs + (q >> 3);
-          const size_t ri = ((size_t)I * P.Nt + (q >> 5)) * 4 + (p >> 3);
-          ready = ld_relaxed_u(P.cnt_col + ci) >= P.exp_col[ci] && ld_relaxed_u(P.cnt_row + ri) >= P.exp_row[ri];
+      {
+        unsigned cc[kLoadBatch], ec[kLoadBatch], cr[kLoadBatch], er[kLoadBatch];
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i) {
+          const int q = next_k + i - p;
+          cc[i] = ec[i] = cr[i] = er[i] = 0;
+          if (next_k + i < kend && vr && q >= 0 && q < n) {
+            const size_t ci = (size_t)I * P.ncs + (q >> 3);
+            const size_t ri = ((size_t)I * P.Nt + (q >> 5)) * 4 + (p >> 3);
+            cc[i] = ld_relaxed_u(P.cnt_col + ci);
+            ec[i] = P.exp_col[ci];
+            cr[i] = ld_relaxed_u(P.cnt_row + ri);
+            er[i] = P.exp_row[ri];
+          }
         }
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i) ready = ready && cc[i] >= ec[i] && cr[i] >= er[i];
       }
       int ab = 0;
       if (lane == 0) ab = aborted(P.hdr) ? 1 : 0;
       ab = __shfl_sync(0xffffffffu, ab, 0);
       if (__all_sync(0xffffffffu, ready) || ab) {
         fence_acquire();
-        for (int k = next_k; k < kend; ++k) {
-          const int q = k - p, f = k % kFar;
-          float2 cf = make_float2(0.f, 0.f), rf = cf;
-          float sc = 1.f;
-          if (vr && q >= 0 && q < n) {
+        float wv[kLoadBatch], sv[kLoadBatch];
+        long long xv[kLoadBatch], gv[kLoadBatch];
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i) {
+          const int q = next_k + i - p;
+          wv[i] = 0.f;
+          sv[i] = 1.f;
+          xv[i] = gv[i] = 0;
+          if (next_k + i < kend && vr && q >= 0 && q < n) {
             const size_t o = (size_t)r * n + q;
-            cf = df_add(make_float2(__ldg(P.W + o), 0.f), df_from_fixed(__ldcg(P.Xc + o), from_units));
-            rf = df_from_fixed(__ldcg(P.Gc + o), from_units);
-            sc = entry_scale(P, r, q);
+            wv[i] = __ldg(P.W + o);
+            xv[i] = __ldcg(P.Xc + o);
+            gv[i] = __ldcg(P.Gc + o);
+            sv[i] = entry_scale(P, r, q);
           }
-          sb.FC[f][p] = cf;
-          sb.FR[f][p] = rf;
-          sb.FS[f][p] = sc;
+        }
+#pragma unroll
+        for (int i = 0; i < kLoadBatch; ++i) {
+          if (next_k + i < kend) {
+            const int f = (next_k + i) % kFar;
+            sb.FC[f][p] = df_add(make_float2(wv[i], 0.f), df_from_fixed(xv[i], from_units));
+            sb.FR[f][p] = df_from_fixed(gv[i], from_units);
+            sb.FS[f][p] = sv[i];
+          }
         }
         __syncwarp();
         __threadfence_block();
@@ -613,7 +655,7 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
         }
         break;
       }
-      __nanosleep(64);
+      __nanosleep(200);
     }
   }
 }

@@ -52,7 +52,7 @@ constexpr int kT = 32;         // band height and tile width
 constexpr int kChunk = 4;      // tiles (bands) per chunk
 constexpr int kSliceLines = 8; // rows (columns) of a slice task's source
 constexpr int kRowAluTiles = 3;  // row terms with d < 3 tiles are the band's own
-constexpr int kGroupsPerTask = 4;  // target groups (128 lines each) per chunk task
+constexpr int kGroupsPerTask = 1;  // target groups (128 lines each) per chunk task
 constexpr int kPrefetch = 16;  // band steps between loading a target's delayed sums and rounding it
 constexpr int kLambda = 48;    // ideal lag of band I behind band I - 1, in steps (queue order only)
 
