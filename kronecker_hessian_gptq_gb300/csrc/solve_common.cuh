@@ -36,8 +36,9 @@ struct Header {
   unsigned maxc_bits;  // max column scale
   float sigma;         // offset of the offset accumulators
   int abort;           // set by a bounded wait that gave up (persistent sweep)
-  unsigned queue_head; // next task of the persistent sweep's task queue
-  int pad[58];
+  unsigned queue_head; // persistent sweep: next ready-queue position to serve
+  unsigned queue_tail; // persistent sweep: next ready-queue position to fill
+  int pad[57];
 };
 static_assert(sizeof(Header) == 256, "header is one alignment unit");
 

@@ -1,7 +1,7 @@
 // sweep.cu -- the BaKron core as one persistent cooperative kernel on
 // sm_103a: a band-by-band sweep of the anti-diagonals on the fp32 pipes
 // (double-float), fed by delayed products on the tensor cores that the same
-// kernel runs from a ready-ordered task queue.
+// kernel runs from a queue of ready tasks.
 //
 // "BaKron: Efficient Quantization with Kronecker-Factored Hessians":
 //   App. B eq. (2): W~_k = W0 + L_B (sum of earlier errors) L_A^T on every
@@ -25,12 +25,14 @@
 //     the step's anti-diagonal rounds it and publishes E and G.
 //   write-out warp: coalesced stores of V, Wq, the bf16 digits of E (row
 //     products) and of G (column products), and the band's G columns for
-//     the band below; publishes the band's progress.
-//   band-above warps (2): fold the previous band's published G columns into
-//     this band (column terms at band distance 1).
+//     the band below; publishes the band's progress and puts the products
+//     whose sources it completed into the ready queue.
+//   loader warp: stages, ahead of the ring, each anti-diagonal's inputs and
+//     delayed sums, and the previous band's published G columns (column
+//     terms at band distance 1, which the ring folds in).
 // Everything farther is carried by tensor-core products that the product
-// warps of every CTA take from a queue ordered by the time their sources
-// complete: slices (8 source lines, K = 32) for the middle distances,
+// warps of every CTA take from the ready queue in the order their sources
+// completed: slices (8 source lines, K = 32) for the middle distances,
 // chunks (K = 128) for the far ones.  They add into two 64-bit fixed-point
 // planes (exact, order-independent integer reductions) and count their
 // completion per target; a band loads a target's delayed sums 16 steps
@@ -99,7 +101,7 @@ struct SweepParams {
   int group, ngroups;
   int32_t* V;
   float* Wq;
-  long long* Xc;         // column-direction delayed sums (fixed point), m x n
+  long long* Xc;         // column-direction delayed sums (fixed point): entry (r, q) at q * m + r
   long long* Gc;         // row-direction delayed sums, m x n
   float2* Gt;            // published G: [band][column][32 rows]
   __nv_bfloat16* EB;     // E digits in source blocks [band][tile][digit][32 rows x 32 columns, core-matrix order]
@@ -110,17 +112,51 @@ struct SweepParams {
   const __nv_bfloat16* FdB;
   int ntA, ntB, nchA, nchB;
   int* progress;         // [Mt]: last band step written out (-1: none)
-  unsigned* cnt_col;     // [Mt][ncs] completed column-direction products per (band, 8 columns)
-  const unsigned* exp_col;
-  unsigned* cnt_row;     // [Mt][Nt][4] completed row-direction products per (band, tile, 8 rows)
-  const unsigned* exp_row;
-  const int* tasks;      // canonical task indices in ready order
-  const unsigned* ntasks;
+  // Completion counters, each started at minus the number of products that
+  // serve its targets (so a target's delayed sums are complete once its
+  // counter, read as a signed int, is >= 0):
+  unsigned* cnt_col;     // [Mt][ncs] column-direction products per (band, 8 columns)
+  unsigned* cnt_row;     // [Mt][Nt][4] row-direction products per (band, tile, 8 rows)
+  const unsigned* rdy_end;  // [Mt * steps]: end of band I's ready list up to step s, at I * steps + s
+  const int* rdy_list;   // canonical task indices per (source band, ready step), in that order
+  unsigned* arrive;      // [column chunks]: source bands that have completed each one's sources
+  int* qslot;            // the ready queue: canonical task indices (-1: not yet filled)
+  unsigned qcap;         // its length (the canonical task count)
+  const unsigned* ntasks;  // tasks in the plan (each enters the ready queue once)
+  long long cc_base;     // canonical index of the first column chunk
   Header* hdr;
   int32_t* status;
   int m, n, Mt, Nt, ncs, bounded, lo, hi;
   Geom geom;
 };
+
+// A task as the product warps use it: its plan entry and derived sizes.
+struct TaskView {
+  Task t;
+  bool row;      // row-direction task (factor L_A, sources E, plane Gc) or column-direction (L_B, G, Xc)
+  int lb;        // first of the task's source lines within the 32-line source block
+  int nslab;     // slabs per group (source tiles or bands along K)
+  int ngroups;
+  int c;         // factor chunk of the source K range
+  int s0;        // first slab within the chunk
+  int tgt0;      // first target line (factor row)
+  int tgt_end;   // one past the last target line
+};
+
+__device__ __noinline__ TaskView view_of(const SweepParams& P, long long idx) {
+  TaskView v;
+  v.t = sweep::decode(P.geom, idx);
+  v.row = v.t.type == sweep::kRowSlice || v.t.type == sweep::kRowChunk;
+  v.lb = v.t.line0 % T;
+  v.nslab = (v.t.kLen + kSlab - 1) / kSlab;
+  const int dlim = v.row ? P.n : P.m;
+  v.tgt0 = T * v.t.t0;
+  v.tgt_end = min(T * v.t.t1, dlim);
+  v.ngroups = (v.tgt_end - v.tgt0 + kTcM - 1) / kTcM;
+  v.c = v.t.k0 / CK;
+  v.s0 = (v.t.k0 % CK) / kSlab;
+  return v;
+}
 
 // ------------------------------------------------------------- shared memory
 struct ProdSmem {
@@ -129,12 +165,12 @@ struct ProdSmem {
     __nv_bfloat16 B[kDigD * T * kSlab];     // source block: 6 digits x 32 lines x 32 (SBO 512 B)
   } buf[2];
   int4 gdesc[2];        // group in tensor-memory half h: (task, group, last of task, -)
+  TaskView gview[2];    // and its task, decoded once by the scheduler lane
   int unit[2];          // unit in buffer p: 1 first slab of its group, 2 last slab, 4 stop
   uint64_t full[2], empty[2], gfull[2], gempty[2];
   uint64_t gready[2];   // gdesc[h] written (scheduler lane's arrival, a release the epilogue acquires)
   uint64_t edone;       // the epilogue threads' updates of a task are fenced (128 arrivals per task)
   uint32_t tmem_base;
-  int pad[3];
 };
 
 struct BandSmem {
@@ -157,9 +193,9 @@ struct BandSmem {
   int panel;                    // last L_A panel loaded
 };
 
-constexpr size_t kSmemBytes = sizeof(ProdSmem) + sizeof(BandSmem) + 1024;
+constexpr size_t kProdSmemBytes = (sizeof(ProdSmem) + 15) / 16 * 16;  // the band state after it stays 16-byte aligned
+constexpr size_t kSmemBytes = kProdSmemBytes + sizeof(BandSmem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM: at most 227 KB of shared memory");
-static_assert(sizeof(ProdSmem) % 16 == 0, "the band state after it stays 16-byte aligned");
 
 // ------------------------------------------------------------------ waits
 __device__ __forceinline__ long long gtimer() {
@@ -195,18 +231,26 @@ __device__ __noinline__ void raise_timeout(const SweepParams& P) {
   atomicExch(&P.hdr->abort, 1);
 }
 
+// Polls between two looks at the abort flag and the clock in the waits
+// below: the abort flag lives in global memory, and reading it on every poll
+// would put an L2 round trip between the flag turning and the waiter seeing
+// it.
+constexpr unsigned kPollsPerCheck = 256;
+
 // Spins until *p >= v with relaxed loads; the caller fences before reading
 // what the value guards.  False once the wait ran out or the kernel aborts.
 __device__ bool wait_relaxed_ge(const SweepParams& P, const int* p, int v) {
   if (ld_relaxed(p) >= v) return true;
   const long long t0 = gtimer();
-  while (ld_relaxed(p) < v) {
-    if (aborted(P.hdr)) return false;
-    if (gtimer() - t0 > kWaitNs) {
-      raise_timeout(P);
-      return false;
+  for (unsigned it = 1; ld_relaxed(p) < v; ++it) {
+    if (it % kPollsPerCheck == 0) {
+      if (aborted(P.hdr)) return false;
+      if (gtimer() - t0 > kWaitNs) {
+        raise_timeout(P);
+        return false;
+      }
     }
-    __nanosleep(128);
+    __nanosleep(64);
   }
   return true;
 }
@@ -214,11 +258,13 @@ __device__ bool wait_relaxed_ge(const SweepParams& P, const int* p, int v) {
 __device__ bool wait_shared_ge(const SweepParams& P, const int* p, int v) {
   if (*(volatile const int*)p >= v) return true;
   const long long t0 = gtimer();
-  while (*(volatile const int*)p < v) {
-    if (aborted(P.hdr)) return false;
-    if (gtimer() - t0 > kWaitNs) {
-      raise_timeout(P);
-      return false;
+  for (unsigned it = 1; *(volatile const int*)p < v; ++it) {
+    if (it % kPollsPerCheck == 0) {
+      if (aborted(P.hdr)) return false;
+      if (gtimer() - t0 > kWaitNs) {
+        raise_timeout(P);
+        return false;
+      }
     }
     __nanosleep(20);
   }
@@ -232,13 +278,6 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Entry scale fp32(R[r, q / group] t[q]) (1 without scales).
-__device__ __forceinline__ float entry_scale(const SweepParams& P, int r, int q) {
-  float sv = 1.f;
-  if (P.scales) sv = P.scales[(size_t)r * P.ngroups + q / P.group];
-  if (P.cscales) sv = __fmul_rn(sv, P.cscales[q]);
-  return sv;
-}
 
 // The six bf16 digits of a solver value (put_digits) into a source block:
 // line l, depth k of a 32 x 32 block, digit b at element b * 1024 +
@@ -374,8 +413,11 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
     }
     // The source L_A panel of the newest source column s - 1 (row 0's).
     if (s >= 1 && ((s - 1) & (T - 1)) == 0 && ((s - 1) >> 5) < P.Nt) wait_shared_ge(P, &sb.panel, (s - 1) >> 5);
-    if (k0 == s) {
-      if (s >= 1) fold(s - 1, 0, 1);
+    // Step s - 1's errors go into slot 0 first (the owner rounds it next),
+    // then into the other slots; one copy of the fold serves both cases.
+    const bool own = k0 == s;
+    if (s >= 1) fold(s - 1, 0, 1);
+    if (own) {
       // Round anti-diagonal s: entry (p, s - p).
       const int q = s - p;
       float2 e = make_float2(0.f, 0.f), g = e;
@@ -407,7 +449,9 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       if (p == 0) *(volatile int*)&sb.rounded = s;
       skip_until = min(s + kRingBars - 1, steps - 1);
       for (int t = s + 1; t <= skip_until; ++t) bar_arrive(ring_bar(t), kRingWarps * 32);
-      if (s >= 1) fold(s - 1, 1, kSlots);
+    }
+    if (s >= 1) fold(s - 1, 1, kSlots);
+    if (own) {
       // Shift the ring: slot i takes slot i + 1, a new anti-diagonal enters.
 #pragma unroll
       for (int i = 0; i + 1 < kSlots; ++i) {
@@ -425,10 +469,49 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
       cL[kCSlots - 1] = 0.f;
       k0 += 8;
       if (k0 < steps) refresh0(k0);
-    } else if (s >= 1) {
-      fold(s - 1, 0, kSlots);
     }
   }
+}
+
+// Puts the tasks whose sources band I completed up to step s (its list
+// entries [next, end(I, s))) into the ready queue.  A column chunk has
+// several source bands and goes in with the last of them to arrive.  Each
+// lane takes one entry at a time; one atomic reserves the warp's queue
+// positions.  Called by the write-out warp right after it published step s.
+// Each entry is a release store (and each arrival an acquire-release
+// atomic): the source writes of this band, and through the arrivals those
+// of the other source bands, are visible before the entry is.
+__device__ void enqueue_ready(const SweepParams& P, int I, int s, unsigned& next) {
+  const int lane = threadIdx.x & 31;
+  const int steps = P.n + T - 1;
+  const unsigned end = __ldg(P.rdy_end + (size_t)I * steps + s);
+  if (next >= end) return;
+  __syncwarp();
+  for (unsigned b = next; b < end; b += 32) {
+    const unsigned e = b + lane;
+    int id = -1;
+    bool go = false;
+    if (e < end) {
+      id = __ldg(P.rdy_list + e);
+      if (id >= P.cc_base) {
+        const long long local = id - P.cc_base;
+        const int h = (int)(local / ((long long)P.geom.colParts * P.Nt));
+        const int nsrc = min(sweep::kChunk * h + sweep::kChunk, P.Mt) - sweep::kChunk * h;
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(P.arrive + local) : "memory");
+        go = old + 1 == (unsigned)nsrc;
+      } else {
+        go = true;
+      }
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, go);
+    unsigned pos = 0;
+    if (lane == 0 && ballot) pos = atomicAdd(&P.hdr->queue_tail, (unsigned)__popc(ballot));
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    const unsigned at = pos + __popc(ballot & ((1u << lane) - 1u));
+    if (go && at < P.qcap) st_release(P.qslot + at, id);
+  }
+  next = end;
 }
 
 // The write-out warp of band I: V, Wq and the digits of E for every row
@@ -438,6 +521,8 @@ __device__ void band_ring(const SweepParams& P, BandSmem& sb, int I, float sigma
 __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float sigma) {
   const int lane = threadIdx.x & 31;
   const int n = P.n, steps = n + T - 1;
+  // Ready-list position of the band's next task to enqueue.
+  unsigned rdy_next = I > 0 ? __ldg(P.rdy_end + (size_t)I * steps - 1) : 0u;
   const float dsc = pow2f(7 - bound_exp(sigma));
   const int r0 = I * T;
   int issued_panel = 0, ready_panel = 0;  // panel 0 is loaded before the sweep starts
@@ -461,10 +546,14 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
     }
     {  // wait for step s to be rounded
       const long long t0 = gtimer();
-      for (;;) {
+      for (unsigned it = 1;; ++it) {
         int go = 0;  // 1: step s is rounded (or the kernel is aborting), 2: the wait ran out
-        if (lane == 0)
-          go = (*(volatile int*)&sb.rounded >= s || aborted(P.hdr)) ? 1 : (gtimer() - t0 > kWaitNs ? 2 : 0);
+        if (lane == 0) {
+          if (*(volatile int*)&sb.rounded >= s)
+            go = 1;
+          else if (it % kPollsPerCheck == 0)
+            go = aborted(P.hdr) ? 1 : (gtimer() - t0 > kWaitNs ? 2 : 0);
+        }
         go = __shfl_sync(0xffffffffu, go, 0);
         if (go == 2 && lane == 0) raise_timeout(P);
         if (go) break;
@@ -473,6 +562,7 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
     }
     // Row tiles completed at step s: row p completes tile j when it rounds
     // column min(32j + 31, n - 1).
+#pragma unroll 1
     for (int ev = 0; ev < 2; ++ev) {
       int p = -1, j = -1;
       if (ev == 0 && s >= T - 1) {
@@ -509,6 +599,7 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
     // barrier), and the release makes them visible with the new progress.
     if ((s & 3) == 3 || s == steps - 1) {
       if (lane == 0) st_release(P.progress + I, s);
+      enqueue_ready(P, I, s, rdy_next);
     }
   }
 }
@@ -532,7 +623,7 @@ __device__ void band_writeout(const SweepParams& P, BandSmem& sb, int I, float s
 // followed by one acquire fence before the data they guard is read.
 // Every decision of this warp is taken by lane 0 or by a warp vote.
 static_assert(kRingBars <= 8, "the loader's staging window assumes refreshes within 8 steps");
-constexpr int kLoadBatch = 8;
+constexpr int kLoadBatch = 4;
 constexpr int kBagFree = T - 1 - 8 + kRingBars;  // steps after column c' until its band-above slot is free
 
 __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sigma) {
@@ -541,9 +632,13 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
   const int r = I * T + p;
   const bool vr = r < P.m;
   const float from_units = pow2f(fixed_unit_exp(sigma));
+  const unsigned* cnt_col_band = P.cnt_col + (size_t)I * P.ncs;
+  const unsigned* cnt_row_band = P.cnt_row + (size_t)I * P.Nt * 4 + (p >> 3);
+  const float* srow = P.scales ? P.scales + (size_t)r * P.ngroups : nullptr;
   int next_bag = I > 0 ? 0 : n, seen = -1;
   int next_k = 0;
-  long long idle_since = gtimer();
+  long long idle_since = 0;
+  unsigned idle_polls = 0;  // loader passes in a row that staged nothing
   while (next_k < steps || next_bag < n) {
     int rd = 0;
     if (lane == 0) rd = *(volatile int*)&sb.rounded;
@@ -581,71 +676,76 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
       }
     }
     // Inputs and delayed sums of the next batch of anti-diagonals: every
-    // counter of the batch read at once (relaxed), then, when all serving
-    // products have counted, one acquire fence and every data load at once.
+    // counter of the batch read at once (relaxed); the leading anti-diagonals
+    // whose serving products have all counted are staged after one acquire
+    // fence, their data loads issued together.
     const int kend = min(min(steps, next_k + kLoadBatch), rounded + kFar + 1);
     if (next_k < kend) {
-      bool ready = true;
+      int nready = 0;  // leading anti-diagonals of the batch that are ready
       {
-        unsigned cc[kLoadBatch], ec[kLoadBatch], cr[kLoadBatch], er[kLoadBatch];
+        int cc[kLoadBatch], cr[kLoadBatch];
 #pragma unroll
         for (int i = 0; i < kLoadBatch; ++i) {
           const int q = next_k + i - p;
-          cc[i] = ec[i] = cr[i] = er[i] = 0;
+          cc[i] = cr[i] = 0;
           if (next_k + i < kend && vr && q >= 0 && q < n) {
-            const size_t ci = (size_t)I * P.ncs + (q >> 3);
-            const size_t ri = ((size_t)I * P.Nt + (q >> 5)) * 4 + (p >> 3);
-            cc[i] = ld_relaxed_u(P.cnt_col + ci);
-            ec[i] = P.exp_col[ci];
-            cr[i] = ld_relaxed_u(P.cnt_row + ri);
-            er[i] = P.exp_row[ri];
+            cc[i] = ld_relaxed(reinterpret_cast<const int*>(cnt_col_band + (q >> 3)));
+            cr[i] = ld_relaxed(reinterpret_cast<const int*>(cnt_row_band + (q >> 5) * 4));
           }
         }
 #pragma unroll
-        for (int i = 0; i < kLoadBatch; ++i) ready = ready && cc[i] >= ec[i] && cr[i] >= er[i];
+        for (int i = 0; i < kLoadBatch; ++i)
+          if (__all_sync(0xffffffffu, (cc[i] | cr[i]) >= 0) && nready == i) nready = i + 1;
       }
-      int ab = 0;
-      if (lane == 0) ab = aborted(P.hdr) ? 1 : 0;
-      ab = __shfl_sync(0xffffffffu, ab, 0);
-      if (__all_sync(0xffffffffu, ready) || ab) {
+      const int k1 = min(kend, next_k + nready);
+      if (k1 > next_k) {
         fence_acquire();
-        float wv[kLoadBatch], sv[kLoadBatch];
+        float wv[kLoadBatch], rv[kLoadBatch], tv[kLoadBatch];
         long long xv[kLoadBatch], gv[kLoadBatch];
+        // Scale group of the batch's first column of this row, then one
+        // column further per anti-diagonal (no division per entry).
+        const int q0 = max(next_k - p, 0);
+        int grp = q0 / P.group, rem = q0 - grp * P.group;
 #pragma unroll
         for (int i = 0; i < kLoadBatch; ++i) {
           const int q = next_k + i - p;
           wv[i] = 0.f;
-          sv[i] = 1.f;
+          rv[i] = tv[i] = 1.f;
           xv[i] = gv[i] = 0;
-          if (next_k + i < kend && vr && q >= 0 && q < n) {
-            const size_t o = (size_t)r * n + q;
-            wv[i] = __ldg(P.W + o);
-            xv[i] = __ldcg(P.Xc + o);
-            gv[i] = __ldcg(P.Gc + o);
-            sv[i] = entry_scale(P, r, q);
+          if (next_k + i < k1 && vr && q >= 0 && q < n) {
+            wv[i] = __ldg(P.W + (size_t)r * n + q);
+            xv[i] = __ldcg(P.Xc + (size_t)q * P.m + r);
+            gv[i] = __ldcg(P.Gc + (size_t)r * n + q);
+            if (srow) rv[i] = __ldg(srow + grp);
+            if (P.cscales) tv[i] = __ldg(P.cscales + q);
+          }
+          if (q >= 0 && ++rem == P.group) {
+            rem = 0;
+            ++grp;
           }
         }
 #pragma unroll
         for (int i = 0; i < kLoadBatch; ++i) {
-          if (next_k + i < kend) {
+          if (next_k + i < k1) {
             const int f = (next_k + i) % kFar;
             sb.FC[f][p] = df_add(make_float2(wv[i], 0.f), df_from_fixed(xv[i], from_units));
             sb.FR[f][p] = df_from_fixed(gv[i], from_units);
-            sb.FS[f][p] = sv[i];
+            sb.FS[f][p] = __fmul_rn(rv[i], tv[i]);  // fp32(R[r, q / group] t[q]); 1 where absent
           }
         }
         __syncwarp();
         __threadfence_block();
-        if (lane == 0) *(volatile int*)&sb.far_done = kend - 1;
-        next_k = kend;
+        if (lane == 0) *(volatile int*)&sb.far_done = k1 - 1;
+        next_k = k1;
         did = true;
       }
     }
     if (did) {
-      idle_since = gtimer();
+      idle_polls = 0;
     } else {
       int out = 0;
-      if (lane == 0) out = (aborted(P.hdr) || gtimer() - idle_since > kWaitNs) ? 1 : 0;
+      if (++idle_polls == 1) idle_since = gtimer();
+      if (lane == 0 && idle_polls % 64 == 0) out = (aborted(P.hdr) || gtimer() - idle_since > kWaitNs) ? 1 : 0;
       out = __shfl_sync(0xffffffffu, out, 0);
       if (out) {  // nothing could be staged for a second: give up (or the kernel is aborting)
         if (lane == 0 && !aborted(P.hdr)) raise_timeout(P);
@@ -675,33 +775,6 @@ __device__ void band_loader(const SweepParams& P, BandSmem& sb, int I, float sig
 //    its completion for each of its targets.
 // Units of consecutive tasks follow each other without a pause; mbarriers
 // carry every hand-off, and every wait is bounded.
-struct TaskView {
-  Task t;
-  bool row;      // row-direction task (factor L_A, sources E, plane Gc) or column-direction (L_B, G, Xc)
-  int lb;        // first of the task's source lines within the 32-line source block
-  int nslab;     // slabs per group (source tiles or bands along K)
-  int ngroups;
-  int c;         // factor chunk of the source K range
-  int s0;        // first slab within the chunk
-  int tgt0;      // first target line (factor row)
-  int tgt_end;   // one past the last target line
-};
-
-__device__ __forceinline__ TaskView view_of(const SweepParams& P, long long idx) {
-  TaskView v;
-  v.t = sweep::decode(P.geom, idx);
-  v.row = v.t.type == sweep::kRowSlice || v.t.type == sweep::kRowChunk;
-  v.lb = v.t.line0 % T;
-  v.nslab = (v.t.kLen + kSlab - 1) / kSlab;
-  const int dlim = v.row ? P.n : P.m;
-  v.tgt0 = T * v.t.t0;
-  v.tgt_end = min(T * v.t.t1, dlim);
-  v.ngroups = (v.tgt_end - v.tgt0 + kTcM - 1) / kTcM;
-  v.c = v.t.k0 / CK;
-  v.s0 = (v.t.k0 % CK) / kSlab;
-  return v;
-}
-
 // Source block of slab sl of a task: row tasks the E digits of (band, source
 // tile), column tasks the G digits of (column tile, source band); 6 digits x
 // 2 KB, contiguous.
@@ -718,22 +791,26 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
   if (warp == kSchedWarp) {
     if (lane == 0) {
       uint32_t zz = 0, gg = 0;  // slab units and groups issued
+      const unsigned ntasks = *P.ntasks;
+      // Ready-queue position of the next task, taken one task ahead so that
+      // its atomic is in flight while the current task is served.  Every
+      // task in the queue is ready, and every task of the plan enters it
+      // once, so each position is filled in time (the wait is bounded).
+      unsigned qi = atomicAdd(&P.hdr->queue_head, 1u);
       for (;;) {
         int idx = -1;
-        if (!aborted(P.hdr) && !broken) {
-          const unsigned i = atomicAdd(&P.hdr->queue_head, 1u);
-          if (i < *P.ntasks) idx = P.tasks[i];
+        if (!broken && qi < ntasks) {  // (the wait returns false once the kernel aborts)
+          if (wait_relaxed_ge(P, P.qslot + qi, 0)) {
+            idx = ld_relaxed(P.qslot + qi);
+            qi = atomicAdd(&P.hdr->queue_head, 1u);
+            // The sources were written by other CTAs' generic stores; the
+            // bulk copies below read them through the async proxy.
+            fence_acquire();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
         }
-        if (idx >= 0) {
-          const Task t = sweep::decode(P.geom, idx);
-          for (int b = t.srcBand0; b < t.srcBand1; ++b) wait_relaxed_ge(P, P.progress + b, t.readyStep);
-          // The sources were written by other CTAs' generic stores; the bulk
-          // copies below read them through the async proxy.
-          fence_acquire();
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-        }
-        const int ngroups = idx >= 0 ? view_of(P, idx).ngroups : 1;
         const TaskView v = view_of(P, idx >= 0 ? idx : 0);
+        const int ngroups = idx >= 0 ? v.ngroups : 1;
         const __nv_bfloat16* Fd = v.row ? P.FdA : P.FdB;
         const int nt = v.row ? P.ntA : P.ntB;
         for (int gi = 0; gi < ngroups; ++gi) {
@@ -742,6 +819,7 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
           // epilogue finished group gg - 2.
           if (gg >= 2) mbar_wait(&sm.gempty[h], ((gg >> 1) - 1) & 1u, broken);
           sm.gdesc[h] = make_int4(idx, gi, gi == ngroups - 1, 0);
+          sm.gview[h] = v;
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gready[h])) : "memory");
           const int nsl = idx >= 0 ? v.nslab : 1;
           for (int sl = 0; sl < nsl; ++sl) {
@@ -840,7 +918,7 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
       const int4 d = sm.gdesc[h];
       if (d.x < 0 || broken) break;
       tc_fence_after();
-      const TaskView v = view_of(P, d.x);
+      const TaskView v = sm.gview[h];
       const int gi = d.y;
       const int tgt = v.tgt0 + gi * kTcM + rr;  // factor row = target line
       const bool rok = tgt < v.tgt_end;
@@ -850,10 +928,12 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
       const int ex = er + eD - 14 - fexp_unit;
       const float sc = ex >= -126 ? pow2f(min(ex, 127)) : 0.f;
       unsigned long long* plane = reinterpret_cast<unsigned long long*>(v.row ? P.Gc : P.Xc);
-      // Row tasks: Gc[source row][target column tgt]; column tasks:
-      // Xc[target row tgt][source column]; source line = line0 + (q - lb).
-      const size_t obase = v.row ? (size_t)v.t.line0 * P.n + tgt : (size_t)tgt * P.n + v.t.line0;
-      const size_t ostep = v.row ? (size_t)P.n : 1;
+      // Both planes are indexed [source line][target line]: Gc by (source
+      // row, target column), Xc by (source column, target row), so the 32
+      // lanes of a warp (consecutive targets) update 256 contiguous bytes.
+      // Source line = line0 + (q - lb).
+      const size_t ostep = v.row ? (size_t)P.n : (size_t)P.m;
+      const size_t obase = (size_t)v.t.line0 * ostep + tgt;
 #pragma unroll 1
       for (int qb = v.lb; qb < v.lb + v.t.nLines; qb += 8) {
         float lv[kLevels][8];
@@ -861,7 +941,7 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
         for (int l = 0; l < kLevels; ++l)
           tmem_ld(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(256 * h + T * l + qb), lv[l]);
         asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
+#pragma unroll 2
         for (int j = 0; j < 8; ++j) {
           // levels 0..2 exactly, the rest (below 2^-24 of the total) in one fp32 sum
           float2 y = two_sum(lv[0][j], lv[1][j] * 0x1p-8f);
@@ -876,11 +956,14 @@ __device__ void product_role(const SweepParams& P, ProdSmem& sm, float sigma) {
       }
       tc_fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.gempty[h])) : "memory");
-      if (d.z) {  // the task's last group: every update is in L2; count it per target
-        // All 128 epilogue threads fence their updates, arrive on edone and
-        // wait for its phase (bounded), so that no thread arrives for the
-        // next task before this task's phase is complete.
-        __threadfence();
+      if (d.z) {  // the task's last group: count it per target
+        // All 128 epilogue threads arrive on edone after their updates (an
+        // arrive releases at CTA scope) and wait for its phase (bounded), so
+        // that no thread arrives for the next task before this task's phase
+        // is complete.  The counting warp's reductions release at GPU scope;
+        // a release is cumulative over what its thread has observed, so it
+        // publishes the updates of all 128 threads, and only that warp waits
+        // for them to be performed.
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.edone)) : "memory");
         mbar_wait(&sm.edone, ntask_done & 1u, broken);
         if (warp == kEpiWarp0) {  // one warp counts the task's completion
@@ -914,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) sweep_kernel(SweepParams P) {
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sweep_smem_raw) + 1023) & ~uintptr_t(1023));
   ProdSmem& sm = *reinterpret_cast<ProdSmem*>(base);
-  BandSmem& sb = *reinterpret_cast<BandSmem*>(base + sizeof(ProdSmem));
+  BandSmem& sb = *reinterpret_cast<BandSmem*>(base + kProdSmemBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float sigma = P.hdr->sigma;
 
@@ -981,38 +1064,45 @@ __global__ void __launch_bounds__(kThreads, 1) sweep_kernel(SweepParams P) {
   (void)lane;
 }
 
-// ------------------------------------------------------------ task queue
-// The canonical tasks (sweep_plan.h) are sorted by the ideal time at which
-// their sources complete (buckets of 8 steps; order inside a bucket is free,
-// since a task needs no other task that becomes ready within 26 steps of
-// it), and the number of tasks serving each target is counted.
-constexpr int kBucketShift = 3;
+// ------------------------------------------------------------ ready lists
+// Every task of the plan (sweep_plan.h) is listed under each of its source
+// bands at its ready step, the lists ordered by (band, step): a counting
+// sort over the Mt x steps buckets.  After the scatter, bucket (I, s) holds
+// the end of band I's entries up to step s, which is what the write-out
+// warps read to enqueue.  The number of tasks serving each target is
+// counted too.
 
-__global__ void plan_count_kernel(Geom g, unsigned* bucket_cnt, unsigned* exp_col, unsigned* exp_row, int ncs) {
+__global__ void plan_count_kernel(Geom g, unsigned* bucket_cnt, unsigned* cnt_col, unsigned* cnt_row, int ncs,
+                                  unsigned* ntasks) {
   const long long total = sweep::total_tasks(g);
+  const int steps = g.n + T - 1;
+  unsigned live = 0;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const Task t = sweep::decode(g, idx);
     if (t.type == sweep::kEmpty) continue;
-    atomicAdd(bucket_cnt + (sweep::ready_time(t) >> kBucketShift), 1u);
+    ++live;
+    for (int b = t.srcBand0; b < t.srcBand1; ++b) atomicAdd(bucket_cnt + (size_t)b * steps + t.readyStep, 1u);
     if (t.type == sweep::kRowSlice || t.type == sweep::kRowChunk) {
       for (int tt = t.t0; tt < t.t1; ++tt)
-        for (int ps = t.ps0; ps < t.ps1; ++ps) atomicAdd(exp_row + ((size_t)t.a * g.Nt + tt) * 4 + ps, 1u);
+        for (int ps = t.ps0; ps < t.ps1; ++ps) atomicSub(cnt_row + ((size_t)t.a * g.Nt + tt) * 4 + ps, 1u);
     } else {
       for (int b = t.t0; b < t.t1; ++b)
-        for (int cs = t.cs0; cs < t.cs1; ++cs) atomicAdd(exp_col + (size_t)b * ncs + cs, 1u);
+        for (int cs = t.cs0; cs < t.cs1; ++cs) atomicSub(cnt_col + (size_t)b * ncs + cs, 1u);
     }
   }
+  live = __reduce_add_sync(0xffffffffu, live);
+  if ((threadIdx.x & 31) == 0 && live) atomicAdd(ntasks, live);
 }
 
-// Exclusive scan of the bucket counts (one CTA); the total goes to *ntasks.
-__global__ void __launch_bounds__(1024) plan_scan_kernel(unsigned* bucket, int nb, unsigned* ntasks) {
+// Exclusive scan of the bucket counts (one CTA).
+__global__ void __launch_bounds__(1024) plan_scan_kernel(unsigned* bucket, long long nb) {
   __shared__ unsigned part[1024];
   const int tid = threadIdx.x;
-  const int per = (nb + 1023) / 1024;
-  const int b0 = tid * per, b1 = min(b0 + per, nb);
+  const long long per = (nb + 1023) / 1024;
+  const long long b0 = tid * per, b1 = min(b0 + per, nb);
   unsigned s = 0;
-  for (int b = b0; b < b1; ++b) s += bucket[b];
+  for (long long b = b0; b < b1; ++b) s += bucket[b];
   part[tid] = s;
   __syncthreads();
   for (int o = 1; o < 1024; o <<= 1) {
@@ -1022,29 +1112,25 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(unsigned* bucket, int n
     __syncthreads();
   }
   unsigned run = tid ? part[tid - 1] : 0u;
-  for (int b = b0; b < b1; ++b) {
+  for (long long b = b0; b < b1; ++b) {
     const unsigned c = bucket[b];
     bucket[b] = run;
     run += c;
   }
-  if (tid == 1023) *ntasks = part[1023];
 }
 
 __global__ void plan_scatter_kernel(Geom g, unsigned* bucket_off, int* list) {
   const long long total = sweep::total_tasks(g);
+  const int steps = g.n + T - 1;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const Task t = sweep::decode(g, idx);
     if (t.type == sweep::kEmpty) continue;
-    const unsigned pos = atomicAdd(bucket_off + (sweep::ready_time(t) >> kBucketShift), 1u);
-    list[pos] = (int)idx;
+    for (int b = t.srcBand0; b < t.srcBand1; ++b) {
+      const unsigned pos = atomicAdd(bucket_off + (size_t)b * steps + t.readyStep, 1u);
+      list[pos] = (int)idx;
+    }
   }
-}
-
-int num_buckets(const Geom& g) {
-  // The latest ready time: the last band's last step.
-  const long long last = sweep::ideal_time(g.Mt - 1, g.n + T - 2);
-  return (int)(last >> kBucketShift) + 2;
 }
 
 struct DeviceInfo {
@@ -1091,9 +1177,9 @@ cudaError_t device_info(DeviceInfo& out) {
 
 // ------------------------------------------------------------- workspace
 struct SweepLayout {
-  size_t plane, Gt, EB, GB, expA, expB, FdA, FdB, progress, cnt_col, exp_col, cnt_row, exp_row, buckets, list,
-      ntasks, total;
-  int nbuckets;
+  size_t plane, Gt, EB, GB, expA, expB, FdA, FdB, progress, qslot, cnt_col, cnt_row, buckets,
+      ntasks, arrive, list, total;
+  long long nbuckets;
 };
 
 SweepLayout sweep_layout(int64_t m, int64_t n) {
@@ -1118,24 +1204,26 @@ SweepLayout sweep_layout(int64_t m, int64_t n) {
   off += align_up(nchA * (CK / kSlab) * kDigF * ntA * 2048);
   L.FdB = off;
   off += align_up(nchB * (CK / kSlab) * kDigF * ntB * 2048);
+  // From progress up to cnt_col: set to -1 before the solve; from cnt_col
+  // up to list: zeroed.
   L.progress = off;
   off += align_up((size_t)g.Mt * sizeof(int));
+  L.qslot = off;
+  off += align_up((size_t)sweep::total_tasks(g) * sizeof(int));
   const size_t ncs = (size_t)((n + 7) / 8);
   L.cnt_col = off;
   off += align_up((size_t)g.Mt * ncs * sizeof(unsigned));
-  L.exp_col = off;
-  off += align_up((size_t)g.Mt * ncs * sizeof(unsigned));
   L.cnt_row = off;
   off += align_up((size_t)g.Mt * g.Nt * 4 * sizeof(unsigned));
-  L.exp_row = off;
-  off += align_up((size_t)g.Mt * g.Nt * 4 * sizeof(unsigned));
-  L.nbuckets = num_buckets(g);
+  L.nbuckets = (long long)g.Mt * (n + T - 1);
   L.buckets = off;
   off += align_up((size_t)L.nbuckets * sizeof(unsigned));
   L.ntasks = off;
   off += align_up(sizeof(unsigned));
+  L.arrive = off;
+  off += align_up((size_t)g.nCC * sizeof(unsigned));
   L.list = off;
-  off += align_up((size_t)sweep::total_tasks(g) * sizeof(int));
+  off += align_up((size_t)(g.nRS + g.nCS + g.nRC + sweep::kChunk * g.nCC) * sizeof(int));
   L.total = off;
   return L;
 }
@@ -1183,11 +1271,14 @@ cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scale
   P.FdB = reinterpret_cast<const __nv_bfloat16*>(base + lay.FdB);
   P.progress = reinterpret_cast<int*>(base + lay.progress);
   P.cnt_col = reinterpret_cast<unsigned*>(base + lay.cnt_col);
-  P.exp_col = reinterpret_cast<const unsigned*>(base + lay.exp_col);
   P.cnt_row = reinterpret_cast<unsigned*>(base + lay.cnt_row);
-  P.exp_row = reinterpret_cast<const unsigned*>(base + lay.exp_row);
-  P.tasks = reinterpret_cast<const int*>(base + lay.list);
+  P.rdy_end = reinterpret_cast<const unsigned*>(base + lay.buckets);
+  P.rdy_list = reinterpret_cast<const int*>(base + lay.list);
+  P.arrive = reinterpret_cast<unsigned*>(base + lay.arrive);
+  P.qslot = reinterpret_cast<int*>(base + lay.qslot);
+  P.qcap = (unsigned)sweep::total_tasks(P.geom);
   P.ntasks = reinterpret_cast<const unsigned*>(base + lay.ntasks);
+  P.cc_base = P.geom.nRS + P.geom.nCS + P.geom.nRC;
   P.status = status_dev;
   P.m = m;
   P.n = n;
@@ -1198,8 +1289,8 @@ cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scale
   P.lo = al.lo;
   P.hi = al.hi;
 
-  // Zeroed state: status, header, the two planes, the counters and buckets;
-  // progress = -1.  (The source blocks need no clearing: the write-out warp
+  // Zeroed state: status, header, the two planes, the counters, buckets and
+  // arrivals; progress and the ready queue = -1.  (The source blocks need no clearing: the write-out warp
   // writes every entry a product reads along K, zeros past the matrix; lines
   // past the matrix only feed output columns that are never stored.)
   err = cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream);
@@ -1226,9 +1317,10 @@ cudaError_t sweep_launch(const float* W, const float* LA, const float* LB, Scale
     unsigned* bk = reinterpret_cast<unsigned*>(base + lay.buckets);
     const long long ntot = sweep::total_tasks(P.geom);
     const unsigned blocks = (unsigned)std::min<long long>((ntot + 255) / 256, 152 * 16);
-    plan_count_kernel<<<blocks, 256, 0, stream>>>(P.geom, bk, reinterpret_cast<unsigned*>(base + lay.exp_col),
-                                                  reinterpret_cast<unsigned*>(base + lay.exp_row), P.ncs);
-    plan_scan_kernel<<<1, 1024, 0, stream>>>(bk, lay.nbuckets, reinterpret_cast<unsigned*>(base + lay.ntasks));
+    plan_count_kernel<<<blocks, 256, 0, stream>>>(P.geom, bk, reinterpret_cast<unsigned*>(base + lay.cnt_col),
+                                                  reinterpret_cast<unsigned*>(base + lay.cnt_row), P.ncs,
+                                                  reinterpret_cast<unsigned*>(base + lay.ntasks));
+    plan_scan_kernel<<<1, 1024, 0, stream>>>(bk, lay.nbuckets);
     plan_scatter_kernel<<<blocks, 256, 0, stream>>>(P.geom, bk, reinterpret_cast<int*>(base + lay.list));
   }
   err = cudaGetLastError();

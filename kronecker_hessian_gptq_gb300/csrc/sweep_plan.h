@@ -1,7 +1,7 @@
 // sweep_plan.h -- the task plan of the persistent band sweep (sweep.cu):
 // which tensor-core product carries each delayed update, when its sources
 // are complete, and which targets it serves.  Host and device share these
-// functions: the device builds the task queue from them, and a host-side
+// functions: the device builds the per-band ready lists from them, and a host-side
 // check (bakron_sweep_plan_check) verifies on the CPU that every delayed
 // update is carried exactly once and before it is needed.
 //
@@ -25,16 +25,17 @@
 //                   of 4 source tiles) from tile 4h + 7 on (h = chunk);
 //   column terms (same column, source band I', target band I = I' + d):
 //     d = 0         the band's own warps;
-//     d = 1         the band's band-above warps, from the published G of
-//                   band I - 1;
+//     d = 1         the band's own warps, from the published G of band
+//                   I - 1 (staged by its loader warp);
 //     d >= 2        COL_SLICE tasks (one source band x 8 columns) up to band
 //                   4 floor(I'/4) + 5, COL_CHUNK tasks (a chunk of 4 source
 //                   bands x one tile of columns) from band 4h' + 6 on.
-// A task becomes ready when its source band has passed a step (the last
-// source entry rounded and written out); its targets are first needed
-// kPrefetch steps before the first target entry is rounded.  In the ideal
-// schedule band I runs kLambda steps behind band I - 1, which leaves every
-// task tens of steps between the two.
+// A task becomes ready when its source bands have passed a step (the last
+// source entry rounded and written out); the band that completes it puts
+// it into the ready queue.  Its targets are first needed kPrefetch steps
+// before the first target entry is rounded.  In the reference schedule of
+// the plan check, band I runs kLambda steps behind band I - 1, which leaves
+// every task tens of steps between the two.
 #pragma once
 
 #include <stdint.h>
@@ -54,7 +55,7 @@ constexpr int kSliceLines = 8; // rows (columns) of a slice task's source
 constexpr int kRowAluTiles = 3;  // row terms with d < 3 tiles are the band's own
 constexpr int kGroupsPerTask = 1;  // target groups (128 lines each) per chunk task
 constexpr int kPrefetch = 16;  // band steps between loading a target's delayed sums and rounding it
-constexpr int kLambda = 48;    // ideal lag of band I behind band I - 1, in steps (queue order only)
+constexpr int kLambda = 48;    // lag of band I behind band I - 1 in the plan check's reference schedule, in steps
 
 enum TaskType : int { kEmpty = 0, kRowSlice = 1, kColSlice = 2, kRowChunk = 3, kColChunk = 4 };
 
@@ -105,9 +106,12 @@ struct Task {
   int line0, nLines; // source lines: rows (row tasks) or columns (column tasks)
 };
 
-// Decodes canonical task index idx (0 <= idx < total_tasks).  Tasks whose
-// targets or sources fall outside the matrix come back as kEmpty.
-SWEEP_HD Task decode(const Geom& g, long long idx) {
+// Decodes canonical task index idx (0 <= idx < total_tasks < 2^31, which
+// the callers check).  Tasks whose targets or sources fall outside the
+// matrix come back as kEmpty.  32-bit arithmetic throughout.
+SWEEP_HD Task decode(const Geom& g, long long idx_in) {
+  unsigned idx = (unsigned)idx_in;
+  const unsigned Nt = (unsigned)g.Nt;
   Task t;
   t.type = kEmpty;
   t.a = t.b = t.c = 0;
@@ -117,11 +121,12 @@ SWEEP_HD Task decode(const Geom& g, long long idx) {
   t.ps0 = t.ps1 = 0;
   t.cs0 = t.cs1 = 0;
   t.k0 = t.kLen = t.line0 = t.nLines = 0;
-  const int nps = kT / kSliceLines;
-  if (idx < g.nRS) {
+  const unsigned nps = kT / kSliceLines;
+  if (idx < (unsigned)g.nRS) {
     const int ps = (int)(idx % nps);
-    const int j = (int)((idx / nps) % g.Nt);
-    const int I = (int)(idx / ((long long)nps * g.Nt));
+    const unsigned rest = idx / nps;
+    const int j = (int)(rest % Nt);
+    const int I = (int)(rest / Nt);
     const int first = j + kRowAluTiles, last = imin(kChunk * (j / kChunk) + kChunk + kRowAluTiles - 1, g.Nt - 1);
     const int r0 = I * kT + kSliceLines * ps;
     if (first > last || r0 >= g.m) return t;
@@ -135,11 +140,12 @@ SWEEP_HD Task decode(const Geom& g, long long idx) {
     t.line0 = r0; t.nLines = imin(kSliceLines, g.m - r0);
     return t;
   }
-  idx -= g.nRS;
-  if (idx < g.nCS) {
+  idx -= (unsigned)g.nRS;
+  if (idx < (unsigned)g.nCS) {
     const int cs = (int)(idx % nps);
-    const int J = (int)((idx / nps) % g.Nt);
-    const int I = (int)(idx / ((long long)nps * g.Nt));
+    const unsigned rest = idx / nps;
+    const int J = (int)(rest % Nt);
+    const int I = (int)(rest / Nt);
     const int first = I + 2, last = imin(kChunk * (I / kChunk) + kChunk + 1, g.Mt - 1);
     const int c0 = J * kT + kSliceLines * cs;
     if (first > last || c0 >= g.n) return t;
@@ -153,12 +159,13 @@ SWEEP_HD Task decode(const Geom& g, long long idx) {
     t.line0 = c0; t.nLines = imin(kSliceLines, g.n - c0);
     return t;
   }
-  idx -= g.nCS;
-  if (idx < g.nRC) {
-    const int nch = cdiv(g.Nt, kChunk);
-    const int part = (int)(idx % g.rowParts);
-    const int h = (int)((idx / g.rowParts) % nch);
-    const int I = (int)(idx / ((long long)g.rowParts * nch));
+  idx -= (unsigned)g.nCS;
+  if (idx < (unsigned)g.nRC) {
+    const unsigned nch = (unsigned)cdiv(g.Nt, kChunk);
+    const int part = (int)(idx % (unsigned)g.rowParts);
+    const unsigned rest = idx / (unsigned)g.rowParts;
+    const int h = (int)(rest % nch);
+    const int I = (int)(rest / nch);
     const int first = kChunk * h + kChunk + kRowAluTiles;  // 4h + 7
     const int g0 = part * kGroupsPerTask;
     const int t0 = first + kChunk * g0;
@@ -168,16 +175,17 @@ SWEEP_HD Task decode(const Geom& g, long long idx) {
     t.srcBand0 = I; t.srcBand1 = I + 1;
     t.readyStep = imin(kT * kChunk * (h + 1), g.n) - 1 + kT - 1;
     t.t0 = t0; t.t1 = imin(t0 + kChunk * kGroupsPerTask, g.Nt);
-    t.ps0 = 0; t.ps1 = nps;
+    t.ps0 = 0; t.ps1 = (int)nps;
     t.k0 = kT * kChunk * h; t.kLen = imin(kT * kChunk, g.n - t.k0);
     t.line0 = kT * I; t.nLines = imin(kT, g.m - kT * I);
     return t;
   }
-  idx -= g.nRC;
-  if (idx < g.nCC) {
-    const int part = (int)(idx % g.colParts);
-    const int J = (int)((idx / g.colParts) % g.Nt);
-    const int h = (int)(idx / ((long long)g.colParts * g.Nt));
+  idx -= (unsigned)g.nRC;
+  if (idx < (unsigned)g.nCC) {
+    const int part = (int)(idx % (unsigned)g.colParts);
+    const unsigned rest = idx / (unsigned)g.colParts;
+    const int J = (int)(rest % Nt);
+    const int h = (int)(rest / Nt);
     const int first = kChunk * h + kChunk + 2;  // 4h + 6
     const int g0 = part * kGroupsPerTask;
     const int t0 = first + kChunk * g0;
