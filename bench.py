@@ -50,10 +50,10 @@ def alu_peak_tflops(sm_max_mhz: float) -> float:
 # Kernel classes on the tensor cores, with the bf16 multiply-adds their exact
 # digit split performs per algorithmic multiply-add (5 factor digits x 6
 # source digits, the 20 pairs of levels 0..5).  "sweep" is the persistent
-# solve kernel, which runs the whole solve (the band sweep on the fp32 pipes
-# and every product on the tensor cores): its entry is the solve's own rate
-# against the tensor roofline of the precision mode, i.e. the measured bf16
-# peak divided by the 20 digit pairs.
+# solve (--method persistent), one kernel that runs the whole solve (the band
+# sweep on the fp32 pipes and every product on the tensor cores): its entry
+# is the solve's own rate against the tensor roofline of the precision mode,
+# i.e. the measured bf16 peak divided by the 20 digit pairs.
 TENSOR_CLASSES = {"chunk_push": 20, "sweep": 20}
 # Kernel launches of one solve on the persistent sweep: input check, offset,
 # two factor exponent and two factor digit kernels, three task-queue
@@ -542,6 +542,8 @@ def run_ours(args, rank, local_rank, world):
         return run_antidiag(args, p, W, LA, LB, s, ws, out, flush, world, dev)
     if args.method == "gptq":  # row-wise GPTQ: the one-sided case B = I of the same solve
         solve = lambda: bk.gptq(W, LA, s, p.bits, ws=ws, out=out)  # noqa: E731
+    elif args.method == "persistent":  # the same solve as one persistent cooperative kernel
+        solve = lambda: bk.quantize_persistent(W, LA, LB, s, p.bits, ws=ws, out=out)  # noqa: E731
     else:
         solve = lambda: bk.quantize(W, LA, LB, s, p.bits, ws=ws, out=out)  # noqa: E731
     for _ in range(args.warmup):
@@ -577,6 +579,26 @@ def run_ours(args, rank, local_rank, world):
             "gpu_launches": None,
         }
 
+    if args.method == "persistent":
+        cfg = workload_config(p, world)
+        cfg["method"] = "persistent sweep (bakron_quantize_persistent)"
+        step_s = total_ms / args.steps * 1e-3
+        f_alg = float(m) * n * (m + n)
+        # the whole solve against the tensor roofline of the precision mode
+        # (20 bf16 digit-pair multiply-adds per algorithmic multiply-add)
+        roof = roofline_for("sweep", f_alg, step_s * 1e3, measured_peaks())
+        roof["traffic"] = None
+        return {
+            "metric": "persistent BaKron solve time & weights quantized/s per m x n layer", "unit": UNIT,
+            "value": world * m * n * args.steps / (total_ms * 1e-3), "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32x2 double-float; bf16 digit products on tensor cores",
+            "data": "synthetic", "config": cfg, "solve_alg_tflops": f_alg / step_s / 1e12,
+            "us_per_antidiagonal_step": total_ms / args.steps * 1e3 / (m + n - 1), "prep_ms": prep_ms,
+            "cold_prep_ms": cold_prep_ms, "clocks": clocks, "roofline": roof, "e2e": None,
+            "gpu_launches": SWEEP_LAUNCHES * args.steps,
+        }
+
     # Per-kernel timing pass (events around every launch), after the timed region.
     ncls = len(_lib.KERNEL_CLASSES)
     kms = (ctypes.c_double * ncls)()
@@ -591,10 +613,8 @@ def run_ours(args, rank, local_rank, world):
     kernels = {name: {"ms": kms[c], "launches": kl[c], "alg_tflops": (kf[c] / (kms[c] * 1e-3) / 1e12) if kms[c] else 0}
                for c, name in enumerate(_lib.KERNEL_CLASSES)}
     dom = max(range(ncls), key=lambda c: kms[c])
-    if kl[ncls - 1]:  # the persistent sweep
-        launches_per_step = SWEEP_LAUNCHES
-    else:  # launch-per-step schedule: class 0 is two launches per solve
-        launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
+    # launch-per-step schedule: class 0 is two launches per solve
+    launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
 
     # End to end through the host entry point: pinned host inputs in, codes out.
     Wh = torch.from_numpy(p.W).pin_memory()
@@ -658,8 +678,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-grid", type=int, default=100, help="shrink factors of --method scales")
-    ap.add_argument("--method", default="bakron", choices=["bakron", "gptq", "scales", "antidiag", "gram"],
-                    help="bakron (default, the headline); gptq: row-wise GPTQ, the case B = I; scales: the "
+    ap.add_argument("--method", default="bakron", choices=["bakron", "persistent", "gptq", "scales", "antidiag", "gram"],
+                    help="bakron (default, the headline); persistent: the same solve as one persistent "
+                         "cooperative kernel; gptq: row-wise GPTQ, the case B = I; scales: the "
                          "scale search and code packing kernels; antidiag: Algorithm 3 beside BaKron "
                          "(give --config c2 for a short run); gram: Kronecker-factor accumulation")
     args = ap.parse_args(argv)

@@ -46,8 +46,11 @@ extern "C" {
 /* 2: adds the row-wise, antidiagonal, alphabet, scale, packing, Hessian-factor
  * and self-test entry points; the entry points of version 1 are unchanged.
  * 3: bakron_quantize_profile reports five kernel classes (the persistent
- * sweep is class 4); adds bakron_sweep_plan_check. */
-#define BAKRON_ABI_VERSION 3
+ * sweep is class 4); adds bakron_sweep_plan_check.
+ * 4: bakron_quantize runs the tile wavefront on every device (measured
+ * faster than the persistent sweep on every workload); the sweep is
+ * bakron_quantize_persistent, and profile class 4 stays 0. */
+#define BAKRON_ABI_VERSION 4
 
 typedef enum bakron_status {
   BAKRON_OK = 0,
@@ -150,6 +153,26 @@ size_t bakron_quantize_workspace_size(int64_t m, int64_t n);
 int bakron_quantize(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                     int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                     int32_t* status_dev, void* stream);
+
+/* The same solve, arguments, workspace, conventions and codes (Theorem
+ * 3.2: every order of the anti-diagonals that respects the dependencies
+ * gives the V of App. B eq. (2)) as one persistent cooperative kernel: one
+ * CTA per SM; bands of 32 rows sweep their anti-diagonals one step at a
+ * time on the fp32 pipes (double-float) while the same CTAs run the
+ * delayed products (Sec. 3.4/3.5) on the tensor cores from a queue of
+ * tasks whose sources are complete.  CTAs wait on flags that other CTAs
+ * set; every wait is bounded (about a second), and one that runs out sets
+ * BAKRON_DEV_TIMEOUT in *status_dev, after which the kernel finishes
+ * without waiting.  Needs cooperative launch (BAKRON_ERR_CUDA otherwise)
+ * and fewer than 2^31 product tasks (BAKRON_ERR_INVALID_ARG otherwise:
+ * well beyond 2^31 weights).  On a GB300 it is slower than bakron_quantize
+ * on every workload measured (4096 x 4096: 22 ms against 16.7 ms): one
+ * band step costs about 2 us, set by the band's write-out and by the
+ * product warps sharing the SM.
+ */
+int bakron_quantize_persistent(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                               int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                               int32_t* status_dev, void* stream);
 
 /* -------------------------------------------------------- row-wise GPTQ
  * The one-sided case B = I of the same solve: with L_B = I every row of W
@@ -308,11 +331,9 @@ int bakron_pack_codes(const int32_t* V, int64_t m, int64_t n, int bits, uint8_t*
  * check and set-up (including the factors' block exponents), 1 = tile
  * solve (diagonal blocks and the distance-1 neighbours), 2 = mid pushes
  * (single source tiles), 3 = chunk products (batched source tiles, on the
- * tensor cores) -- the classes of the launch-per-step schedule -- and 4 =
- * the persistent sweep, which runs the whole solve (band sweep and every
- * product) in one cooperative launch; its set-up kernels are not timed.
- * A solve runs either schedule, so either classes 0..3 or class 4 are
- * non-zero.  Synchronizes `stream` before it returns; the events add a
+ * tensor cores) -- and 4 = the persistent sweep of
+ * bakron_quantize_persistent, which this entry point does not run (always
+ * 0 here).  Synchronizes `stream` before it returns; the events add a
  * little time to every launch.
  */
 #define BAKRON_KERNEL_CLASSES 5

@@ -11,6 +11,7 @@ Hessians" (arXiv 2608.06291), Sec. 3.
 The calls, each a C ABI entry point of the same name with the prefix bakron_:
   factor, prepare        normalized inverse Cholesky factors L-hat (Sec. 3.2)
   quantize               the BaKron solve (Sec. 3.5, App. B eq. (2))
+  quantize_persistent    the same solve as one persistent cooperative kernel
   quantize_host          the same from and to host memory
   gptq                   the one-sided case B = I (row-wise GPTQ, Sec. 1, Alg. 1)
   antidiag               BaKron-antidiagonal (Sec. 3.2, Alg. 3), the quartic baseline
@@ -33,6 +34,7 @@ __all__ = [
     "factor",
     "prepare",
     "quantize",
+    "quantize_persistent",
     "quantize_host",
     "gptq",
     "antidiag",
@@ -131,6 +133,16 @@ def quantize(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=No
     Returns (V int32, Wq float32, status int32[1]) -- all CUDA tensors; the
     status word is 0 on success (BAKRON_DEV_* bits otherwise).
     """
+    return _quantize("bakron_quantize", W, LA, LB, scales, bits, ws, out, stream)
+
+
+def quantize_persistent(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=None):
+    """The same solve as quantize() as one persistent cooperative kernel
+    (bakron_quantize_persistent); same arguments and results."""
+    return _quantize("bakron_quantize_persistent", W, LA, LB, scales, bits, ws, out, stream)
+
+
+def _quantize(entry, W, LA, LB, scales, bits, ws, out, stream):
     torch = _torch()
     lib = _lib.load()
     m, n = W.shape
@@ -147,9 +159,9 @@ def quantize(W, LA, LB, scales=None, bits: int = 0, ws=None, out=None, stream=No
         V, Wq, status = out
     if ws is None:
         ws = _workspace(lib.bakron_quantize_workspace_size(m, n), W.device)
-    st = lib.bakron_quantize(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
+    st = getattr(lib, entry)(_ptr(W), _ptr(LA), _ptr(LB), _ptr(scales), int(bits), m, n, _ptr(V), _ptr(Wq),
                              _ptr(ws), ws.numel(), _ptr(status), _stream_handle(stream))
-    _lib.check(st, "bakron_quantize")
+    _lib.check(st, entry)
     return V, Wq, status
 
 

@@ -40,6 +40,7 @@ SIGNATURES = {
     "bakron_prepare": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_workspace_size": (_sz, [_i64, _i64]),
     "bakron_quantize": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "bakron_quantize_persistent": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_gptq_workspace_size": (_sz, [_i64, _i64]),
     "bakron_gptq_quantize": (_int, [_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_range": (_int, [_vp, _vp, _vp, _vp, _int, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),

@@ -121,6 +121,20 @@ int bakron_quantize(const float* W, const float* LA, const float* LB, const floa
                                            (cudaStream_t)stream));
 }
 
+int bakron_quantize_persistent(const float* W, const float* LA, const float* LB, const float* scales, int bits,
+                               int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
+                               int32_t* status_dev, void* stream) {
+  if (!W || !LA || !LB || !V || !Wq || !status_dev) return BAKRON_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || m * n >= kMaxElems || !bakron::sweep_supported(m, n)) return BAKRON_ERR_INVALID_ARG;
+  if (!(bits == 0 || (bits >= 2 && bits <= 8))) return BAKRON_ERR_INVALID_ARG;
+  if ((const void*)Wq == (const void*)W || (const void*)V == (const void*)W || (void*)V == (void*)Wq)
+    return BAKRON_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, bakron::kAlign) || ws_bytes < bakron::quantize_workspace_bytes(m, n))
+    return BAKRON_ERR_WORKSPACE;
+  return from_cuda(bakron::sweep_launch(W, LA, LB, bakron::per_row(scales), bakron::alphabet_from_bits(bits), (int)m,
+                                        (int)n, V, Wq, ws, status_dev, (cudaStream_t)stream, nullptr));
+}
+
 size_t bakron_gptq_workspace_size(int64_t m, int64_t n) { return bakron_quantize_workspace_size(m, n); }
 
 int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, int bits, int64_t m, int64_t n,

@@ -1069,28 +1069,6 @@ size_t quantize_workspace_bytes(int64_t m, int64_t n) {
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Scales sc,
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer) {
-  // Two-sided solves run as the persistent band sweep (sweep.cu) wherever
-  // this device can co-schedule its cooperative grid; the launch-per-step
-  // tile wavefront below serves the one-sided case (row-wise GPTQ) and
-  // devices without cooperative launch.
-  if (LB && sweep_supported(m, n)) {
-    float ms = 0.f;
-    cudaError_t e = sweep_launch(W, LA, LB, sc, al, m, n, V, Wq, ws, status_dev, stream, timer ? &ms : nullptr);
-    if (e != cudaErrorCooperativeLaunchTooLarge) {
-      if (timer) {
-        for (int c = 0; c < kKernelClasses; ++c) {
-          timer->ms[c] = 0.0;
-          timer->launches[c] = 0;
-          timer->flops[c] = 0.0;
-        }
-        timer->ms[4] = ms;
-        timer->launches[4] = 1;
-        timer->flops[4] = 2.0 * (double)m * n * ((double)m + n) / 2.0;
-      }
-      return e;
-    }
-    (void)cudaGetLastError();  // not co-schedulable here: take the tile wavefront
-  }
   const WsLayout lay = ws_layout(m, n);
   const bool packed = use_packed_digits(m, n);
   const size_t plane = lay.plane;

@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
                  "bakron_status_string", "bakron_abi_version", "bakron_gptq_quantize",
                  "bakron_antidiag_quantize", "bakron_quantize_range", "bakron_quantize_scaled",
                  "bakron_row_scales", "bakron_pack_codes", "bakron_gram", "bakron_sq_norms", "bakron_damp",
-                 "bakron_selftest_wait_timeout", "bakron_quantize_noalloc"):
+                 "bakron_selftest_wait_timeout", "bakron_quantize_noalloc", "bakron_quantize_persistent"):
         assert need in names
 
 
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.bakron_abi_version() == 3
+    assert lib.bakron_abi_version() == 4
     assert lib.bakron_status_string(0) == b"BAKRON_OK"
     assert lib.bakron_status_string(4) == b"BAKRON_ERR_WORKSPACE"
     assert lib.bakron_status_string(99) == b"BAKRON_ERR_UNKNOWN"
@@ -63,12 +63,13 @@ def test_workspace_sizes(lib):
         lib.bakron_factor_workspace_size(10), lib.bakron_factor_workspace_size(20))
 
 
-def test_quantize_rejects_bad_arguments_before_any_launch(lib):
+@pytest.mark.parametrize("entry", ["bakron_quantize", "bakron_quantize_persistent"])
+def test_quantize_rejects_bad_arguments_before_any_launch(lib, entry):
     W = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
     V, Wq = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
     ws = ctypes.c_void_p(0x100000)
     big = lib.bakron_quantize_workspace_size(8, 8)
-    q = lib.bakron_quantize
+    q = getattr(lib, entry)
     assert q(W, W, W, None, 4, 0, 8, V, Wq, ws, big, W, None) == 1  # m < 1
     assert q(W, W, W, None, 4, 8, 0, V, Wq, ws, big, W, None) == 1  # n < 1
     for bits in (1, 9, -1, 16):

@@ -1,6 +1,8 @@
 """Full-size workloads through the C ABI, in the configuration the benchmark
 times (bakron_prepare + bakron_quantize on the device), against the fp64
-oracle entry by entry: c3 (4096 x 4096), c4 (14336 x 4096), c5 (4096 x 14336).
+oracle entry by entry: c3 (4096 x 4096), c4 (14336 x 4096), c5 (4096 x 14336);
+the persistent solve (bakron_quantize_persistent) on the same factors is
+held to the same bars against the same oracle codes.
 
 For each workload the GPU factors L-hat_A, L-hat_B are compared with the
 oracle's (Cholesky of the inverse in fp64, "BaKron: Efficient Quantization
@@ -44,27 +46,36 @@ def bk():
 
 
 def _solve(bk, p):
+    """GPU factors, then the solve by bakron_quantize and by
+    bakron_quantize_persistent on those factors."""
     import torch
 
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()  # noqa: E731
     LA, LB, info = bk.prepare(dev(p.A), dev(p.B))
-    V, Wq, st = bk.quantize(dev(p.W), LA, LB, None if p.scales is None else dev(p.scales), p.bits)
-    torch.cuda.synchronize()
-    assert info.cpu().tolist() == [0, 0] and int(st.item()) == 0
-    return LA.cpu().numpy(), LB.cpu().numpy(), V.cpu().numpy().astype(np.int64), Wq.cpu().numpy()
+    W, s = dev(p.W), None if p.scales is None else dev(p.scales)
+    out = {}
+    for name, solve in (("wavefront", bk.quantize), ("persistent", bk.quantize_persistent)):
+        V, Wq, st = solve(W, LA, LB, s, p.bits)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, name
+        out[name] = (V.cpu().numpy().astype(np.int64), Wq.cpu().numpy())
+    assert info.cpu().tolist() == [0, 0]
+    return LA.cpu().numpy(), LB.cpu().numpy(), out
 
 
 def _against_oracle(bk, p):
-    LA, LB, V, Wq = _solve(bk, p)
+    LA, LB, out = _solve(bk, p)
     LA64, LB64 = O.factors_of(p.A, p.B)
     check_factor(LA, LA64, p.A)
     check_factor(LB, LB64, p.B)
     Vo, Wqo, _ = O.bakron(p.W, LA=LA64, LB=LB64, scales=p.scales, bits=p.bits)
-    match = O.match_fraction(V, Vo)
-    assert match >= V_MATCH, (p.name, match)
     d_ref = O.distortion(p.W, Wqo, p.A, p.B)
-    d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, p.B)
-    assert abs(d_gpu - d_ref) <= distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL), (p.name, d_gpu, d_ref)
+    tol = distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL)
+    for name, (V, Wq) in out.items():
+        match = O.match_fraction(V, Vo)
+        assert match >= V_MATCH, (p.name, name, match)
+        d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, p.B)
+        assert abs(d_gpu - d_ref) <= tol, (p.name, name, d_gpu, d_ref)
 
 
 @pytest.mark.parametrize("key", ["c3", "c4", "c5"])

@@ -182,10 +182,10 @@ def test_bounded_wait_reports_a_timeout_and_the_context_survives(bk):
     check_against_oracle(p, V, Wq, *O.factors_of(p.A, p.B), "after timeout")
 
 
-def test_two_sided_solves_run_as_the_persistent_sweep(bk):
-    """On a GB300 every two-sided solve is one cooperative sweep launch
-    (profile class 4), not the launch-per-step fallback (classes 0..3), which
-    serves devices that cannot co-schedule the sweep's grid."""
+def test_profile_runs_the_tile_wavefront(bk):
+    """bakron_quantize (and its profiled twin) runs the launch-per-step tile
+    wavefront: tile solves, mid pushes and chunk products (classes 1..3),
+    never the persistent sweep (class 4, bakron_quantize_persistent)."""
     import ctypes
 
     import torch
@@ -193,7 +193,7 @@ def test_two_sided_solves_run_as_the_persistent_sweep(bk):
     from kronecker_hessian_gptq_gb300 import _lib
 
     lib = bk.load_library()
-    p = random_problem(200, 300, bits=4, seed=12)
+    p = random_problem(400, 300, bits=4, seed=12)
     LA64, LB64 = O.factors_of(p.A, p.B)
     W, LA, LB, s = _dev(p.W), _dev(LA64), _dev(LB64), _dev(p.scales)
     ws = torch.empty(bk.quantize_workspace_size(p.m, p.n), dtype=torch.uint8, device="cuda")
@@ -206,6 +206,5 @@ def test_two_sided_solves_run_as_the_persistent_sweep(bk):
                                      V.data_ptr(), Wq.data_ptr(), ws.data_ptr(), ws.numel(), st.data_ptr(),
                                      torch.cuda.current_stream().cuda_stream, kms, kl, kf)
     assert rc == 0 and int(st.item()) == 0
-    assert list(kl) == [0, 0, 0, 0, 1], list(kl)
-    assert abs(kf[4] - float(p.m) * p.n * (p.m + p.n)) < 1.0
-    check_against_oracle(p, V.cpu().numpy().astype(np.int64), Wq.cpu().numpy(), LA64, LB64, "sweep profile")
+    assert kl[1] > 0 and kl[2] > 0 and kl[3] > 0 and kl[4] == 0, list(kl)
+    check_against_oracle(p, V.cpu().numpy().astype(np.int64), Wq.cpu().numpy(), LA64, LB64, "wavefront profile")
