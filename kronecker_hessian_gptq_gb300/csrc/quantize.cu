@@ -537,7 +537,8 @@ __global__ void __launch_bounds__(256) mid_push_kernel(QParams P, int K, int I0)
 // 2^(e_r + eD - 14).
 constexpr int kTcM = 128;        // target rows per group (UC target tiles)
 constexpr int UC = kTcM / T;
-constexpr int kGroupsPerCta = 8;  // target groups one chunk product CTA works through
+constexpr int kMaxItems = 16;  // (candidate, target group) items one chunk product CTA works through
+constexpr int kItemsPerCand = 8;  // items per CTA when each CTA serves one candidate (packed digits)
 
 // Chunk product candidates closed by tile anti-diagonal K: for every column
 // J whose tile (K - J, J) closes a chunk of B tile rows, and every row I
@@ -615,21 +616,29 @@ template <bool kPacked>
 struct TcSmem : TcStage<kPacked> {
   __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
   __nv_bfloat16 Bd[kDigD * T * CK];         // source digits, 192 rows (digit-major) x CK, SBO 2048 B
-  int er[kGroupsPerCta][kTcM];              // row exponents of each group's factor block
+  signed char er[kMaxItems][kTcM];          // row exponents of each item's factor block
+  ChunkCand cand[kMaxItems];                // the candidate of each item
+  int grp[kMaxItems];                       // its target group within the candidate
+  int seg[kMaxItems];                       // 1 where an item starts a new candidate (after the first)
+  int count;                                // items mapped (the CTA's share of the launch)
   uint64_t full[2];                         // digit slab p ready (producer arrivals / bulk-copy bytes)
   uint64_t empty[2];                        // products reading digit slab p done (commit)
   uint64_t grp_full[2];                     // products of a group in tensor-memory half h done (commit)
   uint64_t grp_empty[2];                    // epilogue of tensor-memory half h done (epilogue arrivals)
+  uint64_t bd_free;                         // products reading the source digits of a candidate done (commit)
+  uint64_t bd_full;                         // the next candidate's source digits loaded (copier arrivals)
   uint32_t tmem_base;
 };
 
-// Chunk products closed by tile anti-diagonal K.  blockIdx.x: candidate;
-// CTA y = blockIdx.y works through the target groups y, y + gridDim.y, ...
-// (at most kGroupsPerCta), each 128 target rows.  Column products:
+// Chunk products closed by tile anti-diagonal K.  The work of a launch is
+// the list of items (candidate t, target group g of 128 target rows),
+// ordered by candidate and then group, G items in all; CTA b takes the
+// items G b / gridDim.x .. G (b + 1) / gridDim.x - 1 (at most kMaxItems),
+// so that one wave of CTAs shares the launch evenly.  Column products:
 //   Xc[targets, J] += L_B[targets, chunk rows] G[chunk rows, J];
 // row products, as their transpose:
 //   Gc[I, targets]^T += L_A[targets, chunk cols] E[I, chunk cols]^T.
-// Warp-specialized pipeline over the k-slabs of all groups of the CTA:
+// Warp-specialized pipeline over the k-slabs of all items of the CTA:
 //  * the next slab's five factor digit blocks go into one of two digit
 //    buffers once the products that read that buffer are done: bulk copies
 //    of the packed digits by one thread, or fp32 slabs copied two ahead
@@ -641,43 +650,102 @@ struct TcSmem : TcStage<kPacked> {
 //  * epilogue warps turn each finished group's six levels into fixed-point
 //    updates of the plane, while the next group is multiplied in the other
 //    tensor-memory half.
+// The source digits of one candidate stay in shared memory for all of its
+// items; where a CTA's items pass into the next candidate, the products of
+// the last item commit bd_free, the copiers load the next candidate's
+// digits and arrive on bd_full, and the products wait for it.
 // Handshakes are mbarriers; every wait is bounded.
 // (At most 80 registers: 30 K registers, so that a tile solve fits beside
 // it; its shared memory admits one per SM.)
 template <bool kPacked>
-__global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col) {
+__device__ __forceinline__ void load_source_digits(const QParams& P, TcSmem<kPacked>& sm, const ChunkCand& cc,
+                                                   int copier, int ncopiers) {
+  const __nv_bfloat16* dp = cc.col ? P.DGt : P.DE;
+  const size_t pst = cc.col ? P.dstrideG : P.dstrideE;
+  const int ld = cc.col ? P.ldG : P.ldE;
+  const int qlim = cc.col ? P.n : P.m, klim = cc.col ? P.m : P.n;
+  const int q0 = cc.col ? cc.J * T : cc.I * T;
+  for (int e = copier; e < kDigD * T * (CK / 8); e += ncopiers) {
+    const int b = e / (T * (CK / 8));
+    const int q = (e / (CK / 8)) % T;
+    const int k8 = 8 * (e % (CK / 8));
+    const int gq = q0 + q, gk = cc.c * CK + k8;
+    const bool ok = gq < qlim && gk < klim;
+    const __nv_bfloat16* p = dp + (ok ? b * pst + (size_t)gq * ld + gk : 0);
+    const int row = b * T + q;  // stacked digit-major
+    unsigned char* dst = reinterpret_cast<unsigned char*>(sm.Bd) + (row / 8) * 2048 + (k8 / 8) * 128 + (row % 8) * 16;
+    cp_async(dst, p, ok ? 16 : 0, 16);
+  }
+  cp_async_commit();
+}
+
+template <bool kPacked>
+__global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col, int ncand, int nitems,
+                                                int per_cand) {
   using Shape = TcShape<kPacked>;
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem<kPacked>& sm = *reinterpret_cast<TcSmem<kPacked>*>(tc_smem_raw);
-  ChunkCand cc;
-  if (!chunk_candidate(P, K, ncand_col, blockIdx.x, cc)) return;
-  const int ngroups = (cc.ntiles + UC - 1) / UC;
-  const int g0 = blockIdx.y, gstep = gridDim.y;
-  if (g0 >= ngroups) return;
-  const int mygroups = min(kGroupsPerCta, (ngroups - 1 - g0) / gstep + 1);
+  const int i0 = (int)(((long long)blockIdx.x * nitems) / gridDim.x);
+  const int i1 = (int)(((long long)(blockIdx.x + 1) * nitems) / gridDim.x);
+  // the host sizes the grid so that a CTA's share is at most kMaxItems
+  const int mygroups = per_cand ? per_cand : min(i1 - i0, kMaxItems);
+  if (mygroups <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   static_assert(Shape::kWarps >= kTcEpiWarp0 + 4 && kTcCopyWarp < kTcEpiWarp0,
                 "warp roles: MMA, copies or producers, 4 epilogue warps");
+  // Item map: candidate and group of each of this CTA's items.
+  if (tid == 0 && per_cand) {
+    // Per candidate: CTA (t, y) takes groups y, y + gridDim.y, ... of
+    // candidate t = blockIdx.x (at most per_cand of them).
+    ChunkCand c;
+    int k = 0;
+    if (chunk_candidate(P, K, ncand_col, blockIdx.x, c)) {
+      const int ng = (c.ntiles + UC - 1) / UC;
+      for (int g = blockIdx.y; g < ng && k < mygroups; g += gridDim.y, ++k) {
+        sm.cand[k] = c;
+        sm.grp[k] = g;
+        sm.seg[k] = 0;
+      }
+    }
+    sm.count = k;
+  } else if (tid == 0) {
+    int first = 0, k = 0;  // first item index of candidate t
+    for (int t = 0; t < ncand && k < mygroups; ++t) {
+      ChunkCand c;
+      if (!chunk_candidate(P, K, ncand_col, t, c)) continue;
+      const int ng = (c.ntiles + UC - 1) / UC;
+      for (int g = max(i0 + k - first, 0); g < ng && k < mygroups; ++g, ++k) {
+        sm.cand[k] = c;
+        sm.grp[k] = g;
+        sm.seg[k] = k > 0 ? 1 : 0;
+        if (k > 0 && g > 0) sm.seg[k] = 0;
+      }
+      first += ng;
+    }
+    sm.count = k;  // equal to mygroups when the host's item count matches the candidates
+  }
+  __syncthreads();
+  const int nitems_cta = sm.count;
+  if (nitems_cta <= 0) return;
   const bool is_epi = warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4;
   const bool is_prod = !kPacked && warp != kTcMmaWarp && !is_epi;
   const int ptid = is_prod ? (warp < kTcEpiWarp0 ? tid - 32 : tid - 160) : -1;  // 0 .. kProducers-1
-  const float* F = cc.col ? P.LB : P.LA;
-  const __nv_bfloat16* Fd = cc.col ? P.FdB : P.FdA;
-  const int nt = cc.col ? P.ntB : P.ntA;
-  const signed char* fexp = cc.col ? P.expB : P.expA;
-  const int d = cc.col ? P.m : P.n;
-  const int nch = cc.col ? P.nchB : P.nchA;
   constexpr int nslab = CK / kSlab;
-  const int nz = mygroups * nslab;  // slabs of all groups, in order
-  auto group_row0 = [&](int gi) { return (cc.first + (g0 + gi * gstep) * UC) * T; };
-  auto group_rows = [&](int gi) { return min(kTcM, (cc.first + cc.ntiles) * T - group_row0(gi)); };
+  const int nz = nitems_cta * nslab;  // slabs of all items, in order
+  auto group_row0 = [&](int gi) { return (sm.cand[gi].first + sm.grp[gi] * UC) * T; };
+  auto group_rows = [&](int gi) {
+    return min(kTcM, (sm.cand[gi].first + sm.cand[gi].ntiles) * T - group_row0(gi));
+  };
 
   // Producer item it (of kTcM * kSlab / 8): row it / 4, columns 8 (it mod 4) .. +7.
   auto copy_slab = [&](int z) {
     if constexpr (!kPacked) {
-      const bool vec4 = (d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0;
       if (z < nz) {
         const int gi = z / nslab, s = z % nslab;
+        const ChunkCand& cc = sm.cand[gi];
+        const float* F = cc.col ? P.LB : P.LA;
+        const int d = cc.col ? P.m : P.n;
+        const bool vec4 = (d % 4) == 0 && (reinterpret_cast<uintptr_t>(F) & 15) == 0;
         const int row0 = group_row0(gi), rows = group_rows(gi);
         for (int it = ptid; it < kTcM * kSlab / 8; it += Shape::kProducers) {
           const int r = it / 4, k8 = 8 * (it % 4);
@@ -704,36 +772,25 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
     }
   };
 
-  // Prologue: source digits (written by the tile solves; by all threads, or
-  // by the producers), row exponents, mbarriers, tensor memory; without
-  // packed digits also the first two fp32 slabs.
+  // Prologue: source digits of the first item's candidate (written by the
+  // tile solves; by all threads, or by the producers), row exponents,
+  // mbarriers, tensor memory; without packed digits also the first two fp32
+  // slabs.
   const int copier = kPacked ? tid : ptid;
   const int ncopiers = kPacked ? Shape::kThreads : Shape::kProducers;
   if (copier >= 0) {
-    const __nv_bfloat16* dp = cc.col ? P.DGt : P.DE;
-    const size_t pst = cc.col ? P.dstrideG : P.dstrideE;
-    const int ld = cc.col ? P.ldG : P.ldE;
-    const int qlim = cc.col ? P.n : P.m, klim = cc.col ? P.m : P.n;
-    const int q0 = cc.col ? cc.J * T : cc.I * T;
-    for (int e = copier; e < kDigD * T * (CK / 8); e += ncopiers) {
-      const int b = e / (T * (CK / 8));
-      const int q = (e / (CK / 8)) % T;
-      const int k8 = 8 * (e % (CK / 8));
-      const int gq = q0 + q, gk = cc.c * CK + k8;
-      const bool ok = gq < qlim && gk < klim;
-      const __nv_bfloat16* p = dp + (ok ? b * pst + (size_t)gq * ld + gk : 0);
-      const int row = b * T + q;  // stacked digit-major
-      unsigned char* dst = reinterpret_cast<unsigned char*>(sm.Bd) + (row / 8) * 2048 + (k8 / 8) * 128 + (row % 8) * 16;
-      cp_async(dst, p, ok ? 16 : 0, 16);
-    }
-    cp_async_commit();
+    load_source_digits(P, sm, sm.cand[0], copier, ncopiers);
     copy_slab(0);
     copy_slab(1);
   }
-  for (int e = tid; e < mygroups * kTcM; e += blockDim.x) {
+  for (int e = tid; e < nitems_cta * kTcM; e += blockDim.x) {
     const int gi = e / kTcM, r = e % kTcM;
+    const ChunkCand& cc = sm.cand[gi];
     const int gr = group_row0(gi) + r;
-    sm.er[gi][r] = gr < d ? (int)fexp[(size_t)gr * nch + cc.c] : -100;
+    const int d = cc.col ? P.m : P.n;
+    const signed char* fexp = cc.col ? P.expB : P.expA;
+    const int nch = cc.col ? P.nchB : P.nchA;
+    sm.er[gi][r] = gr < d ? fexp[(size_t)gr * nch + cc.c] : (signed char)-100;
   }
   if (tid == 0) {
 #pragma unroll
@@ -744,6 +801,9 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.grp_full[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.grp_empty[i])));
     }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.bd_free)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.bd_full)),
+                 "r"(kPacked ? 32 : Shape::kProducers));
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == kTcMmaWarp) {  // two tensor-memory halves of 256 columns (6 levels x 32 used in each)
@@ -761,42 +821,62 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
   const uint32_t tmem = sm.tmem_base;
   const int eD = bound_exp(P.hdr->sigma);
   bool broken = false;
+  // Source digits of the candidate starting at item gi (gi > 0, sm.seg[gi]):
+  // once the products of the previous candidate are done (bd_free, phase
+  // nseg - 1), the copiers load them and arrive on bd_full.
+  auto next_sources = [&](int gi, uint32_t nseg, int cp, int ncp) {
+    mbar_wait(&sm.bd_free, (nseg - 1) & 1u, broken);
+    load_source_digits(P, sm, sm.cand[gi], cp, ncp);
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.bd_full)) : "memory");
+  };
 
   if (kPacked ? warp == kTcCopyWarp : is_prod) {
     if constexpr (kPacked) {
-      if (lane == 0) {
-        // Slab z of group gi: for each digit a, the group's tiles (at most
-        // UC) are contiguous 2 KB blocks of the packed digits: one bulk copy.
-        for (int z = 0; z < nz; ++z) {
-          const int p = z & 1, gi = z / nslab, s = z % nslab;
+      // Slab z of item gi: for each digit a, the group's tiles (at most UC)
+      // are contiguous 2 KB blocks of the packed digits: one bulk copy by
+      // lane 0.  The whole warp loads the next candidate's source digits.
+      uint32_t nseg = 0;
+      for (int z = 0; z < nz; ++z) {
+        const int p = z & 1, gi = z / nslab, s = z % nslab;
+        if (s == 0 && sm.seg[gi]) next_sources(gi, ++nseg, lane, 32);
+        if (lane == 0) {
+          const ChunkCand& cc = sm.cand[gi];
+          const __nv_bfloat16* Fd = cc.col ? P.FdB : P.FdA;
+          const int nt = cc.col ? P.ntB : P.ntA;
           const int t0 = group_row0(gi) / T;
           const int ntg = min(UC, nt - t0);
           const uint32_t bytes = (uint32_t)ntg * 2048u;
           if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
-          if (broken) break;
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[p])),
-                       "r"(bytes * kDigF)
-                       : "memory");
-          const size_t cs = (size_t)cc.c * nslab + s;
+          if (!broken) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[p])),
+                         "r"(bytes * kDigF)
+                         : "memory");
+            const size_t cs = (size_t)cc.c * nslab + s;
 #pragma unroll
-          for (int a = 0; a < kDigF; ++a) {
-            const unsigned char* src =
-                reinterpret_cast<const unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t0) * 2048;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                    smem_u32(sm.A[p][a])),
-                "l"(src), "r"(bytes), "r"(smem_u32(&sm.full[p]))
-                : "memory");
+            for (int a = 0; a < kDigF; ++a) {
+              const unsigned char* src =
+                  reinterpret_cast<const unsigned char*>(Fd) + ((cs * kDigF + a) * nt + t0) * 2048;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                      smem_u32(sm.A[p][a])),
+                  "l"(src), "r"(bytes), "r"(smem_u32(&sm.full[p]))
+                  : "memory");
+            }
           }
         }
+        __syncwarp();
+        if (__shfl_sync(0xffffffffu, broken ? 1 : 0, 0)) break;
       }
-      __syncwarp();
     } else {
+      uint32_t nseg = 0;
       for (int z = 0; z < nz; ++z) {
-        const int p = z & 1, gi = z / nslab;
+        const int p = z & 1, gi = z / nslab, s = z % nslab;
         copy_slab(z + 2);
         asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // this thread's items of slab z
         if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+        if (s == 0 && sm.seg[gi]) next_sources(gi, ++nseg, ptid, Shape::kProducers);
         for (int it = ptid; it < kTcM * kSlab / 8; it += Shape::kProducers) {
           const int r = it / 4, k8 = 8 * (it % 4);
           const float sc = pow2f(7 - sm.er[gi][r]);
@@ -828,9 +908,11 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
     }
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) {
+      uint32_t nseg = 0;
       for (int z = 0; z < nz; ++z) {
         const int p = z & 1, gi = z / nslab, s = z % nslab, h = gi & 1;
         if (s == 0 && gi >= 2) mbar_wait(&sm.grp_empty[h], (uint32_t)((gi >> 1) - 1) & 1u, broken);
+        if (s == 0 && sm.seg[gi]) mbar_wait(&sm.bd_full, nseg++ & 1u, broken);
         mbar_wait(&sm.full[p], (uint32_t)(z >> 1) & 1u, broken);
         if (broken) break;
         tc_fence_after();
@@ -845,17 +927,21 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col)
           }
         }
         umma_commit(&sm.empty[p]);
-        if (s == nslab - 1) umma_commit(&sm.grp_full[h]);
+        if (s == nslab - 1) {
+          umma_commit(&sm.grp_full[h]);
+          if (gi + 1 < nitems_cta && sm.seg[gi + 1]) umma_commit(&sm.bd_free);
+        }
       }
     }
     __syncwarp();
   } else if (warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + 4) {  // epilogue warps
     const int qd = warp - kTcEpiWarp0;  // tensor-memory lane quarter
     const int r = 32 * qd + lane;       // output row of this thread within the group
-    for (int gi = 0; gi < mygroups; ++gi) {
+    for (int gi = 0; gi < nitems_cta; ++gi) {
       const int h = gi & 1;
       mbar_wait(&sm.grp_full[h], (uint32_t)(gi >> 1) & 1u, broken);
       tc_fence_after();
+      const ChunkCand& cc = sm.cand[gi];
       const int row0 = group_row0(gi), rows = group_rows(gi);
       // levels -> value: 2^(e_r + eD - 14); value -> fixed-point units: 2^-unit_exp
       const int ex = sm.er[gi][r] + eD - 14 - fixed_unit_exp(P.hdr->sigma);
@@ -970,6 +1056,13 @@ class LaunchClock {
 constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
 template <bool kPacked>
 constexpr int kChunkSmem = (int)sizeof(TcSmem<kPacked>);
+// A tile solve (43008 bytes of static shared memory) must fit beside one
+// chunk product CTA on an SM (228 KB, 1 KB reserved per CTA): the solve
+// chain would otherwise wait for whole chunk CTAs to finish before each of
+// its launches.
+static_assert(sizeof(TcSmem<false>) + 43008 + 2048 <= 228 * 1024 &&
+                  sizeof(TcSmem<true>) + 43008 + 2048 <= 228 * 1024,
+              "a tile solve must fit beside a chunk product CTA");
 
 // Chunk launches of consecutive tile anti-diagonals go round-robin over
 // kChunkStreams streams.  With more than one they overlap and may update
@@ -982,7 +1075,8 @@ constexpr int kChunkStreams = 1;
 struct StreamSet {
   bool ready = false;
   unsigned long long ctx_id = 0;  // context the streams and events belong to
-  cudaStream_t mid = nullptr, chunk[kChunkStreams] = {};
+  cudaStream_t solve = nullptr, mid = nullptr, chunk[kChunkStreams] = {};
+  int sms = 0;  // multiprocessors of the device
   std::vector<cudaEvent_t> ev;
 };
 constexpr int kMaxDevices = 128;
@@ -1003,12 +1097,18 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     // the largest block of work and their stream sets the pace (measured on
     // c3: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms here).
     (void)lo;
+    e = cudaStreamCreateWithPriority(&S.solve, cudaStreamNonBlocking, hi);
+    if (e != cudaSuccess) return e;
     e = cudaStreamCreateWithPriority(&S.mid, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
     for (int i = 0; i < kChunkStreams; ++i) {
       e = cudaStreamCreateWithPriority(&S.chunk[i], cudaStreamNonBlocking, hi);
       if (e != cudaSuccess) return e;
     }
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&S.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kChunkSmem<false>);
     if (e != cudaSuccess) return e;
@@ -1133,6 +1233,12 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   // With a timer every kernel runs on the caller's stream, one after the
   // other, so that each event pair brackets one kernel alone.
   cudaStream_t s_mid = timer ? stream : S.mid;
+  // Layers up to 2^24 weights: the tile solves run on a stream of the
+  // highest priority, beside the products (measured on 4096 x 4096: 15.9
+  // against 16.6 ms); on larger layers the products set the pace, and the
+  // solves stay on the caller's stream (measured on 14336 x 4096: 66.7
+  // against 80.9 ms).
+  cudaStream_t s_solve = (timer || packed) ? stream : S.solve;
   auto s_chunk = [&](int K) { return timer ? stream : S.chunk[K % kChunkStreams]; };
 
   LaunchClock clock(timer);
@@ -1169,6 +1275,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   cudaEventRecord(ev_start, stream);
   cudaStreamWaitEvent(s_mid, ev_start, 0);
   for (int i = 0; i < kChunkStreams; ++i) cudaStreamWaitEvent(s_chunk(i), ev_start, 0);
+  if (s_solve != stream) cudaStreamWaitEvent(s_solve, ev_start, 0);
 
   const double t3 = (double)T * T * T;
   std::vector<char> mid_on(Kmax + 1, 0), chunk_on(Kmax + 1, 0);
@@ -1179,16 +1286,16 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     const int I0 = P.skew ? std::max(0, K - (P.Nt - 1)) : 0;
     const int I1 = P.skew ? std::min(K, P.Mt - 1) : P.Mt - 1;
     const int nsrc = I1 - I0 + 1;
-    if (K >= 2 && mid_on[K - 2]) cudaStreamWaitEvent(stream, ev_mid[K - 2], 0);
+    if (K >= 2 && mid_on[K - 2]) cudaStreamWaitEvent(s_solve, ev_mid[K - 2], 0);
     // One wait each is enough: mid(K-2) follows every earlier mid launch on
     // its stream, every chunk launch before chunk(K-B-1) was waited for by an
     // earlier solve (the solves are in order on one stream), and a missing
     // launch was covered by the wait of an earlier solve.
-    if (K >= B + 1 && chunk_on[K - B - 1]) cudaStreamWaitEvent(stream, ev_chunk[K - B - 1], 0);
-    clock.begin(1, stream);
-    tile_solve_kernel<<<nsrc, kSolveThreads, 0, stream>>>(P, K, I0);
+    if (K >= B + 1 && chunk_on[K - B - 1]) cudaStreamWaitEvent(s_solve, ev_chunk[K - B - 1], 0);
+    clock.begin(1, s_solve);
+    tile_solve_kernel<<<nsrc, kSolveThreads, 0, s_solve>>>(P, K, I0);
     clock.end(2.0 * 3.5 * t3 * nsrc);  // in-tile sums, L_B[I,I] row part, two distance-1 pulls
-    cudaEventRecord(ev_solve[K], stream);
+    cudaEventRecord(ev_solve[K], s_solve);
 
     // mid pushes from the sources of K
     double mid_tiles = 0;
@@ -1212,14 +1319,16 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     const int ncc = (LB && std::min(K, P.Mt - 1) >= B - 1) ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
     const int ncr = P.skew ? (std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0)
                            : ((K + 1) % B == 0 ? P.Mt : 0);  // tile columns: every row closes a chunk
+    // The same candidates as chunk_candidate, and their items (target groups).
     double chunk_tiles = 0;
-    int chunk_most = 0;  // most targets of one candidate
+    int nitems = 0, most = 0;  // items (target groups) in all; most of one candidate
     for (int t = 0; t < ncc; ++t) {
       const int J = K - (B - 1) - B * t, last = K - J;
       if (J >= 0 && J < P.Nt && last < P.Mt) {
         const int nt = std::max(0, P.Mt - (last / B + 2) * B);
         chunk_tiles += nt;
-        chunk_most = std::max(chunk_most, nt);
+        nitems += (nt + UC - 1) / UC;
+        most = std::max(most, (nt + UC - 1) / UC);
       }
     }
     for (int t = 0; t < ncr; ++t) {
@@ -1227,20 +1336,32 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
       if (I >= 0 && I < P.Mt && last < P.Nt) {
         const int nt = std::max(0, P.Nt - (last / B + 2) * B);
         chunk_tiles += nt;
-        chunk_most = std::max(chunk_most, nt);
+        nitems += (nt + UC - 1) / UC;
+        most = std::max(most, (nt + UC - 1) / UC);
       }
     }
     if (chunk_tiles > 0) {
       cudaStreamWaitEvent(s_chunk(K), ev_solve[K], 0);
-      const int groups = (chunk_most + UC - 1) / UC;
-      const int ctas = (groups + kGroupsPerCta - 1) / kGroupsPerCta;  // CTAs per candidate
       clock.begin(3, s_chunk(K));
-      if (packed)
+      if (packed) {
+        // Each CTA serves one candidate, at most kItemsPerCand of its groups.
+        const int ctas = (most + kItemsPerCand - 1) / kItemsPerCand;
         chunk_tc_kernel<true><<<dim3(ncc + ncr, ctas), TcShape<true>::kThreads, kChunkSmem<true>, s_chunk(K)>>>(
-            P, K, ncc);
-      else
-        chunk_tc_kernel<false><<<dim3(ncc + ncr, ctas), TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
-            P, K, ncc);
+            P, K, ncc, ncc + ncr, nitems, kItemsPerCand);
+      } else {
+        // The launch's items shared evenly: small launches over at most
+        // three quarters of the SMs (one CTA each), so that the next tile
+        // solves find SMs without a chunk product CTA; large ones in whole
+        // waves of one CTA per SM; at most kMaxItems items per CTA.
+        const int cap = std::max(1, S.sms * 3 / 4);
+        int ctas = std::min(nitems, cap);
+        if (nitems > cap * kMaxItems) {
+          const int waves = (nitems + S.sms * kMaxItems - 1) / (S.sms * kMaxItems);
+          ctas = std::min(nitems, S.sms * waves);
+        }
+        chunk_tc_kernel<false><<<ctas, TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
+            P, K, ncc, ncc + ncr, nitems, 0);
+      }
       clock.end(2.0 * B * t3 * chunk_tiles);
       cudaEventRecord(ev_chunk[K], s_chunk(K));
       chunk_on[K] = 1;
@@ -1248,6 +1369,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     }
   }
   // Join: the caller's stream covers all side work of this call.
+  if (s_solve != stream) cudaStreamWaitEvent(stream, ev_solve[Kmax], 0);
   if (last_mid >= 0) cudaStreamWaitEvent(stream, ev_mid[last_mid], 0);
   for (int i = 0; i < kChunkStreams; ++i)
     if (last_chunk[i] >= 0) cudaStreamWaitEvent(stream, ev_chunk[last_chunk[i]], 0);
