@@ -18,8 +18,15 @@
 // the column operand unless the tile is diagonal and unweighted; its low
 // half with weights), one
 // thread issues an MMA of M = N = 128, K = 16 per 16 samples into tensor
-// memory (fp32; every bf16 x bf16 product is exact there), and four warps
-// read the tile out and write it and its mirror.
+// memory (fp32; every bf16 x bf16 product is exact there).  The fp32
+// accumulation in tensor memory is restarted every kGSegSamples samples:
+// after each segment four epilogue warps add the accumulator into a running
+// fp32 sum kept in tensor memory (columns 128..255), 32 columns per round
+// trip, while the MMAs wait, so the rounding of the tensor cores' long
+// accumulation grows with the segment length instead of with N (the running
+// sum adds one rounding per segment).  Two CTAs share an SM, so one
+// multiplies while the other adds.  After the last segment the epilogue
+// writes the tile and its mirror.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -35,6 +42,8 @@ namespace {
 constexpr int kGT = 128;                 // output tile edge (tensor-memory lanes, MMA N)
 constexpr int kGK = 64;                  // samples per stage: 8 groups of 8 (16 bytes)
 constexpr int kGStages = 3;
+constexpr int kGSegStages = 16;                 // stages per accumulation segment
+constexpr int kGSegSamples = kGSegStages * 64;  // 1024 samples
 constexpr int kGWarps = 8;
 constexpr int kGThreads = kGWarps * 32;
 constexpr uint32_t kGLbo = 128;              // stride of an 8-sample group within an 8-row block
@@ -44,11 +53,13 @@ constexpr int kGChunks = kGT * (kGK / 8);    // 16-byte chunks per block: 1024
 
 template <bool kW>
 struct GramSmem {
-  alignas(128) unsigned char A[kGStages][kGTileBytes];
-  alignas(128) unsigned char B[kGStages][kW ? 2 : 1][kGTileBytes];
-  uint64_t full[kGStages];
-  uint64_t empty[kGStages];
-  uint64_t done;
+  static constexpr int kStages = kGStages;
+  alignas(128) unsigned char A[kStages][kGTileBytes];
+  alignas(128) unsigned char B[kStages][kW ? 2 : 1][kGTileBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t seg_full;   // the MMAs of a segment are done (commit)
+  uint64_t seg_empty;  // the epilogue has added the segment into the running sum (128 arrivals)
   uint32_t tmem_base;
 };
 
@@ -130,7 +141,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 template <bool kW>
-__global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
+__global__ void __launch_bounds__(kGThreads, 2) gram_kernel(GramParams P) {
   extern __shared__ __align__(1024) unsigned char g_smem_raw[];
   GramSmem<kW>& sm = *reinterpret_cast<GramSmem<kW>*>(g_smem_raw);
   int bi, bj;
@@ -141,16 +152,20 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   const int nz = P.nkb;
   bool broken = false;
 
+  constexpr int kStages = GramSmem<kW>::kStages;
+  const int nseg = (nz + kGSegStages - 1) / kGSegStages;
+
   if (tid == 0) {
-    for (int i = 0; i < kGStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.full[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
     }
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.done)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.seg_full)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.seg_empty)));
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;\n" ::"r"(smem_u32(&sm.tmem_base)));
+  if (warp == 0) {  // the accumulator at column 0, the running sum at column 128
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(smem_u32(&sm.tmem_base)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   tc_fence_before();
@@ -162,8 +177,8 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
     const uint32_t bytes = (uint32_t)kGTileBytes * (1u + (copy_b ? 1u : 0u) + (kW ? 1u : 0u));
     const size_t rowa = (size_t)bi * P.nkb, rowb = (size_t)bj * P.nkb;
     for (int z = 0; z < nz; ++z) {
-      const int slot = z % kGStages;
-      if (z >= kGStages) mbar_wait(&sm.empty[slot], (uint32_t)((z / kGStages) - 1) & 1u, broken);
+      const int slot = z % kStages;
+      if (z >= kStages) mbar_wait(&sm.empty[slot], (uint32_t)((z / kStages) - 1) & 1u, broken);
       if (broken) break;
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[slot])),
                    "r"(bytes)
@@ -175,8 +190,12 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   } else if (warp == 0 && lane == 0) {  // the MMA thread
     constexpr uint32_t idesc = umma_idesc_bf16(kGT, kGT);
     for (int z = 0; z < nz; ++z) {
-      const int slot = z % kGStages;
-      mbar_wait(&sm.full[slot], (uint32_t)(z / kGStages) & 1u, broken);
+      const int slot = z % kStages;
+      const int seg = z / kGSegStages, zs = z % kGSegStages;
+      const uint32_t acc = tmem;
+      // the accumulator is free once the epilogue added segment seg - 1
+      if (zs == 0 && seg >= 1) mbar_wait(&sm.seg_empty, (uint32_t)(seg - 1) & 1u, broken);
+      mbar_wait(&sm.full[slot], (uint32_t)(z / kStages) & 1u, broken);
       if (broken) break;
       tc_fence_after();
       const uint32_t a0 = smem_u32(sm.A[slot]);
@@ -185,12 +204,12 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
       for (int j = 0; j < kGK / 16; ++j) {
         const uint32_t off = (uint32_t)(2 * j) * kGLbo;
         const uint64_t da = umma_sdesc(a0 + off, kGLbo, kGSbo);
-        umma_bf16(tmem, da, umma_sdesc(b0 + off, kGLbo, kGSbo), idesc, (z > 0 || j > 0) ? 1u : 0u);
-        if (kW) umma_bf16(tmem, da, umma_sdesc(smem_u32(sm.B[slot][kW ? 1 : 0]) + off, kGLbo, kGSbo), idesc, 1u);
+        umma_bf16(acc, da, umma_sdesc(b0 + off, kGLbo, kGSbo), idesc, (zs > 0 || j > 0) ? 1u : 0u);
+        if (kW) umma_bf16(acc, da, umma_sdesc(smem_u32(sm.B[slot][kW ? 1 : 0]) + off, kGLbo, kGSbo), idesc, 1u);
       }
       umma_commit(&sm.empty[slot]);
+      if (zs == kGSegStages - 1 || z == nz - 1) umma_commit(&sm.seg_full);
     }
-    umma_commit(&sm.done);
   }
   __syncwarp();
 
@@ -198,25 +217,53 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
     const int q = warp - 4;
     const int r = 32 * q + lane;
     const int i = bi * kGT + r;
-    mbar_wait(&sm.done, 0u, broken);
-    tc_fence_after();
-    for (int c8 = 0; c8 < kGT / 8; ++c8) {
-      float v[8];
-      tmem_ld(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(8 * c8), v);
-      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-      // Entry (i, j) and its mirror (j, i); a diagonal tile writes its lower
-      // triangle and mirrors it, so G is exactly symmetric even where the
-      // two triangles' products were rounded differently (weighted split).
-      if (i < P.d && !broken) {
+    const uint32_t lanes = (uint32_t)(32 * q) << 16;
+    for (int seg = 0; seg < nseg; ++seg) {
+      const bool last = seg == nseg - 1;
+      mbar_wait(&sm.seg_full, (uint32_t)seg & 1u, broken);
+      tc_fence_after();
+#pragma unroll 1
+      for (int c32 = 0; c32 < kGT / 32; ++c32) {
+        // Running sum += this segment's sums (one fp32 rounding per segment),
+        // 32 columns per round trip to tensor memory.
+        float v[4][8], hi[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = bj * kGT + 8 * c8 + e;
-          if (j >= P.d || (diag && j > i)) break;
-          float g = P.alpha * v[e];
-          if (P.beta != 0.f) g = fmaf(P.beta, P.G[(size_t)i * P.d + j], g);
-          P.G[(size_t)i * P.d + j] = g;
-          if (j != i) P.G[(size_t)j * P.d + i] = g;  // the mirror (coalesced across the warp)
+        for (int k = 0; k < 4; ++k) {
+          tmem_ld(tmem + lanes + (uint32_t)(32 * c32 + 8 * k), v[k]);
+          if (seg > 0) tmem_ld(tmem + lanes + (uint32_t)(kGT + 32 * c32 + 8 * k), hi[k]);
         }
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) hi[k][e] = seg == 0 ? v[k][e] : hi[k][e] + v[k][e];
+        if (!last) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_st(tmem + lanes + (uint32_t)(kGT + 32 * c32 + 8 * k), hi[k]);
+          continue;
+        }
+        // Entry (i, j) and its mirror (j, i); a diagonal tile writes its lower
+        // triangle and mirrors it, so G is exactly symmetric even where the
+        // two triangles' products were rounded differently (weighted split).
+        if (i < P.d && !broken) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = bj * kGT + 32 * c32 + 8 * k + e;
+              if (j < P.d && !(diag && j > i)) {
+                float g = P.alpha * hi[k][e];
+                if (P.beta != 0.f) g = fmaf(P.beta, P.G[(size_t)i * P.d + j], g);
+                P.G[(size_t)i * P.d + j] = g;
+                if (j != i) P.G[(size_t)j * P.d + i] = g;  // the mirror (coalesced across the warp)
+              }
+            }
+        }
+      }
+      if (!last) {
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        tc_fence_before();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.seg_empty)) : "memory");
       }
     }
   }
@@ -224,7 +271,7 @@ __global__ void __launch_bounds__(kGThreads) gram_kernel(GramParams P) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;\n" ::"r"(tmem));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tmem));
 }
 
 __global__ void sq_norms_kernel(const uint16_t* Y, int m, int N, int ldy, float* w) {
