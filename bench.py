@@ -159,8 +159,14 @@ class ClockSampler:
 
 
 def load_workload(key: str):
-    from workloads import make_config
+    """A named workload (c1 .. c5), or "rand:MxN": an M x N layer with
+    damped Gaussian Gram factors, W ~ N(0, 0.02^2) and 4-bit per-row scales
+    (the shape of a layer without a named workload)."""
+    from workloads import make_config, random_problem
 
+    if key.startswith("rand:"):
+        m, n = (int(x) for x in key[5:].lower().split("x"))
+        return random_problem(m, n, bits=4, seed=m + 7 * n, w_std=0.02)
     return make_config(key)
 
 
@@ -672,7 +678,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="c3")
+    ap.add_argument("--config", default="c3", help="c1 .. c5, or rand:MxN for a random layer of that shape")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
