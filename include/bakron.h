@@ -129,8 +129,9 @@ int bakron_prepare(const float* A, const float* B, int64_t m, int64_t n, float* 
  */
 
 /* Workspace bytes bakron_quantize needs for an m x n problem: about 72 per
- * weight, plus, on layers above 2^24 weights, 10 per entry of each factor
- * (the factors' digits, computed once per solve for the chunk products). */
+ * weight, plus, on layers of 2^22 weights and more, 10 per entry of each
+ * factor (the factors' digits, computed once per solve for the chunk
+ * products). */
 size_t bakron_quantize_workspace_size(int64_t m, int64_t n);
 
 /* W: device, m x n; read only.

@@ -587,16 +587,19 @@ constexpr int kTcEpiWarp0 = 4;          // warps 4..7: epilogue, tensor-memory l
 constexpr int kTcStages = 3;            // fp32 factor slabs in flight per producer (digits made in the kernel)
 constexpr int kEpiCols = 8;             // output columns per epilogue step (registers: 6 levels each)
 
-// Two ways to feed the factor digits.  Packed (layers above 2^24 weights):
-// the digits are computed once per solve (factor_digits_kernel) and each
-// slab arrives as five bulk copies, 8 warps.  In the kernel (smaller
+// Two ways to feed the factor digits.  Packed (layers of 2^22 weights and
+// more): the digits are computed once per solve (factor_digits_kernel) and
+// each slab arrives as five bulk copies, 8 warps.  In the kernel (smaller
 // layers): 7 producer warps copy fp32 factor slabs with cp.async and split
 // them into digits, 12 warps.  Packed reads 10 bytes per factor entry
-// instead of 4 and runs the products faster alone; on 4096 x 4096, where the
-// solve chain and not the products sets the pace, its heavier traffic slowed
-// the chain more than it gained (16.7-17.4 ms against 16.6 ms on one GPU),
-// on 14336 x 4096 it gains 15% (66.8 against 78.6 ms).
-inline bool use_packed_digits(int64_t m, int64_t n) { return m * n > ((int64_t)1 << 24); }
+// instead of 4 but needs no producer warps; measured on one GB300:
+// 4096 x 4096 14.7 ms against 15.8 ms, 14336 x 4096 66.8 against 78.6 ms;
+// 1024 x 1024 is the same either way.
+inline bool use_packed_digits(int64_t m, int64_t n) { return m * n >= ((int64_t)1 << 22); }
+// Layers above 2^24 weights, where the chunk products set the pace: one
+// candidate per chunk-product CTA, and the tile solves on the caller's
+// stream (see quantize_launch).
+inline bool large_layer(int64_t m, int64_t n) { return m * n > ((int64_t)1 << 24); }
 
 template <bool kPacked>
 struct TcShape {
@@ -1238,7 +1241,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   // against 16.6 ms); on larger layers the products set the pace, and the
   // solves stay on the caller's stream (measured on 14336 x 4096: 66.7
   // against 80.9 ms).
-  cudaStream_t s_solve = (timer || packed) ? stream : S.solve;
+  cudaStream_t s_solve = (timer || large_layer(m, n)) ? stream : S.solve;
   auto s_chunk = [&](int K) { return timer ? stream : S.chunk[K % kChunkStreams]; };
 
   LaunchClock clock(timer);
@@ -1343,11 +1346,15 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     if (chunk_tiles > 0) {
       cudaStreamWaitEvent(s_chunk(K), ev_solve[K], 0);
       clock.begin(3, s_chunk(K));
-      if (packed) {
+      if (large_layer(m, n)) {
         // Each CTA serves one candidate, at most kItemsPerCand of its groups.
         const int ctas = (most + kItemsPerCand - 1) / kItemsPerCand;
-        chunk_tc_kernel<true><<<dim3(ncc + ncr, ctas), TcShape<true>::kThreads, kChunkSmem<true>, s_chunk(K)>>>(
-            P, K, ncc, ncc + ncr, nitems, kItemsPerCand);
+        if (packed)
+          chunk_tc_kernel<true><<<dim3(ncc + ncr, ctas), TcShape<true>::kThreads, kChunkSmem<true>, s_chunk(K)>>>(
+              P, K, ncc, ncc + ncr, nitems, kItemsPerCand);
+        else
+          chunk_tc_kernel<false><<<dim3(ncc + ncr, ctas), TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
+              P, K, ncc, ncc + ncr, nitems, kItemsPerCand);
       } else {
         // The launch's items shared evenly: small launches over at most
         // three quarters of the SMs (one CTA each), so that the next tile
@@ -1359,8 +1366,12 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
           const int waves = (nitems + S.sms * kMaxItems - 1) / (S.sms * kMaxItems);
           ctas = std::min(nitems, S.sms * waves);
         }
-        chunk_tc_kernel<false><<<ctas, TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
-            P, K, ncc, ncc + ncr, nitems, 0);
+        if (packed)
+          chunk_tc_kernel<true><<<ctas, TcShape<true>::kThreads, kChunkSmem<true>, s_chunk(K)>>>(
+              P, K, ncc, ncc + ncr, nitems, 0);
+        else
+          chunk_tc_kernel<false><<<ctas, TcShape<false>::kThreads, kChunkSmem<false>, s_chunk(K)>>>(
+              P, K, ncc, ncc + ncr, nitems, 0);
       }
       clock.end(2.0 * B * t3 * chunk_tiles);
       cudaEventRecord(ev_chunk[K], s_chunk(K));

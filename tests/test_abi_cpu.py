@@ -203,16 +203,14 @@ def test_selftest_rejects_a_missing_status_word(lib):
 
 
 def test_workspace_holds_packed_factor_digits_only_on_large_layers(lib):
-    """Above 2^24 weights the solve adds the factors' packed digits (10 bytes
-    per factor entry, 2 KB blocks of 32 rows x 32 columns x 5 digits per
-    128-column chunk)."""
+    """From 2^22 weights on the solve adds the factors' packed digits (10
+    bytes per factor entry, 2 KB blocks of 32 rows x 32 columns x 5 digits
+    per 128-column chunk)."""
     def packed(d):
         nch, nt = -(-d // 128), -(-d // 32)
         return -(-(nch * 4 * 5 * nt * 2048) // 256) * 256
 
-    base = lib.bakron_quantize_workspace_size(4096, 4096)  # exactly 2^24 weights: digits made in the kernel
-    assert lib.bakron_quantize_workspace_size(4096, 4097) > base
-    w1 = lib.bakron_quantize_workspace_size(4104, 4096)  # above: packed digits for both factors
-    w0 = lib.bakron_quantize_workspace_size(4096, 4096)
-    assert w1 - w0 >= packed(4104) + packed(4096)
-    assert lib.bakron_gptq_workspace_size(4104, 4096) == w1
+    below = lib.bakron_quantize_workspace_size(2048, 2047)  # 2^22 - 2048 weights: digits made in the kernel
+    at = lib.bakron_quantize_workspace_size(2048, 2048)  # 2^22 weights: packed digits for both factors
+    assert at - below >= packed(2048) + packed(2048)
+    assert lib.bakron_quantize_workspace_size(4104, 4096) > lib.bakron_quantize_workspace_size(4096, 4096)

@@ -14,9 +14,10 @@ defines the one correct V): at least 99.99% identical, distortion within
 generation and the oracle on the host cores).
 
 Ragged shapes that reach the chunk products of the solve (more than two
-chunks of tile rows and columns, edges not multiples of 32), and one layer
-above 2^24 weights that is not a multiple of 128 (the packed factor-digit
-variant of the chunk products), are compared the same way.
+chunks of tile rows and columns, edges not multiples of 32) are compared the
+same way: below 2^22 weights (digits made in the chunk kernel), between 2^22
+and 2^24 (packed factor digits, items shared evenly over the CTAs), and
+above 2^24 (packed digits, one candidate per CTA).
 """
 
 import numpy as np
@@ -83,7 +84,8 @@ def test_full_size_against_oracle(bk, key):
     _against_oracle(bk, make_config(key))
 
 
-@pytest.mark.parametrize("m,n,bits", [(1000, 1300, 3), (1300, 1000, 3), (4100, 4100, 4)])
+@pytest.mark.parametrize("m,n,bits", [(1000, 1300, 3), (1300, 1000, 3), (2100, 2100, 4), (4100, 4100, 4)])
 def test_ragged_chunk_shapes_against_oracle(bk, m, n, bits):
-    # 4100 x 4100 = 16.81 M weights > 2^24: the packed factor digits.
+    # 2100 x 2100 = 4.41 M weights >= 2^22: packed digits, shared items;
+    # 4100 x 4100 = 16.81 M weights > 2^24: packed digits, one candidate per CTA.
     _against_oracle(bk, random_problem(m, n, bits=bits, seed=m + 7 * n, w_std=0.02))
