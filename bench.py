@@ -619,8 +619,11 @@ def run_ours(args, rank, local_rank, world):
     kernels = {name: {"ms": kms[c], "launches": kl[c], "alg_tflops": (kf[c] / (kms[c] * 1e-3) / 1e12) if kms[c] else 0}
                for c, name in enumerate(_lib.KERNEL_CLASSES)}
     dom = max(range(ncls), key=lambda c: kms[c])
-    # launch-per-step schedule: class 0 is two launches per solve
-    launches_per_step = 2 * kl[0] + sum(kl[c] for c in range(1, ncls))
+    # launch-per-step schedule: the set-up class (one timed span) is the input
+    # check, the offset, the two factors' block exponents and, from 2^22 weights
+    # on, their packed digits; then every tile solve, mid push and chunk product
+    setup_launches = 4 + (2 if m * n >= (1 << 22) else 0)
+    launches_per_step = setup_launches * kl[0] + sum(kl[c] for c in range(1, ncls))
 
     # End to end through the host entry point: pinned host inputs in, codes out.
     Wh = torch.from_numpy(p.W).pin_memory()

@@ -65,21 +65,28 @@ def _solve(bk, p):
 
 
 def _against_oracle(bk, p):
+    """Asserts the bars and prints one line per solve (pytest -s shows them):
+    codes identical, distortions, and the factors' largest error as a
+    fraction of their bound."""
     LA, LB, out = _solve(bk, p)
     LA64, LB64 = O.factors_of(p.A, p.B)
-    check_factor(LA, LA64, p.A)
-    check_factor(LB, LB64, p.B)
+    fa = check_factor(LA, LA64, p.A)
+    fb = check_factor(LB, LB64, p.B)
     Vo, Wqo, _ = O.bakron(p.W, LA=LA64, LB=LB64, scales=p.scales, bits=p.bits)
     d_ref = O.distortion(p.W, Wqo, p.A, p.B)
     tol = distortion_tolerance(d_ref, Wqo, p.A, p.B, D_REL)
     for name, (V, Wq) in out.items():
         match = O.match_fraction(V, Vo)
-        assert match >= V_MATCH, (p.name, name, match)
         d_gpu = O.distortion(p.W, Wq.astype(np.float64), p.A, p.B)
+        same = int(np.count_nonzero(V == Vo))
+        print(f"\nparity {p.name} {p.m}x{p.n} b{p.bits} {name}: codes identical {same} of {V.size} ({match:.8f}); "
+              f"distortion {d_gpu:.10g} vs oracle {d_ref:.10g} (rel {abs(d_gpu - d_ref) / max(abs(d_ref), 1e-300):.2g}); "
+              f"factor error / bound: L_A {fa:.3g}, L_B {fb:.3g}")
+        assert match >= V_MATCH, (p.name, name, match)
         assert abs(d_gpu - d_ref) <= tol, (p.name, name, d_gpu, d_ref)
 
 
-@pytest.mark.parametrize("key", ["c3", "c4", "c5"])
+@pytest.mark.parametrize("key", ["c2", "c3", "c4", "c5"])
 def test_full_size_against_oracle(bk, key):
     _against_oracle(bk, make_config(key))
 
