@@ -107,15 +107,18 @@ __host__ __device__ __forceinline__ int mid_end(int s) { return (s / B + 2) * B;
 
 // Solves every tile (I, K - skew I), I = I0 + blockIdx.x, of step K (a tile
 // anti-diagonal, or with L_B = I a tile column).
-// 512 threads; lane p owns the two entries (p, q_j) of tile row p with
-// p + q_j = 2 w + j (mod 32), j = 0, 1, w the warp: the entries of one
-// anti-diagonal sit in one warp and one slot j, so only that warp runs the
-// rounding step while the others accumulate.
-constexpr int kSolveThreads = 512;
-constexpr int kPer = T * T / kSolveThreads;  // entries per thread (2)
-constexpr int kRows = kSolveThreads / T;     // rows per pass of the natural mapping (16)
-
+// kSolveThreads threads (1024 or 512); lane p owns the kPer = 1024 /
+// kSolveThreads entries (p, q_j) of tile row p with p + q_j = kPer w + j
+// (mod 32), j < kPer, w the warp: the entries of one anti-diagonal sit in
+// one warp and one slot j, so only that warp runs the rounding step while
+// the others accumulate.  Measured on one GB300: 1024 threads solve 4096 x
+// 4096 in 14.2 ms against 14.7 ms with 512 (256: 19.3 ms); on 14336 x 4096,
+// where a 1024-thread solve leaves no room on its SM for a chunk product
+// CTA, 512 threads are faster (67.1 against 68.8 ms).
+template <int kSolveThreads>
 __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, int K, int I0) {
+  constexpr int kPer = T * T / kSolveThreads;  // entries per thread
+  constexpr int kRows = kSolveThreads / T;     // rows per pass of the natural mapping
   const int I = I0 + blockIdx.x;
   const int J = K - P.skew * I;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1296,7 +1299,10 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
     // launch was covered by the wait of an earlier solve.
     if (K >= B + 1 && chunk_on[K - B - 1]) cudaStreamWaitEvent(s_solve, ev_chunk[K - B - 1], 0);
     clock.begin(1, s_solve);
-    tile_solve_kernel<<<nsrc, kSolveThreads, 0, s_solve>>>(P, K, I0);
+    if (large_layer(m, n))
+      tile_solve_kernel<512><<<nsrc, 512, 0, s_solve>>>(P, K, I0);
+    else
+      tile_solve_kernel<1024><<<nsrc, 1024, 0, s_solve>>>(P, K, I0);
     clock.end(2.0 * 3.5 * t3 * nsrc);  // in-tile sums, L_B[I,I] row part, two distance-1 pulls
     cudaEventRecord(ev_solve[K], s_solve);
 
