@@ -136,6 +136,22 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
   const float sigma = P.hdr->sigma;
   const float from_units = pow2f(fixed_unit_exp(sigma));
 
+  // Each entry's scale in the skewed mapping below (lane p = tile row, slot
+  // j = column qj[j]): its row (group) scale times its column scale,
+  // rounded once to fp32, and its reciprocal for the rounding decision;
+  // loaded first, so that their latency overlaps the loads below.
+  float se[kPer], rcpe[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int pr = I * T + lane;
+    const int c = J * T + ((kPer * warp + j - lane) & (T - 1));
+    float sv = 1.f;
+    if (pr < P.m && c < P.n) {
+      if (P.scales) sv = P.scales[(size_t)pr * P.ngroups + c / P.group];
+      if (P.cscales) sv = __fmul_rn(sv, P.cscales[c]);
+    }
+    se[j] = sv;
+  }
   // Loads in the natural mapping: rows a = warp + kRows t, column b = lane.
   const int b = lane;
   const int cb = J * T + b;
@@ -211,20 +227,8 @@ __global__ void __launch_bounds__(kSolveThreads) tile_solve_kernel(QParams P, in
       for (int j = 0; j < kPer; ++j) acc[j].mac(l, sA[i][qj[j]]);
     }
   }
-  // Each entry's scale: its row (group) scale times its column scale,
-  // rounded once to fp32; and its reciprocal for the rounding decision.
-  float se[kPer], rcpe[kPer];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int c = J * T + qj[j];
-    float sv = 1.f;
-    if (vr && c < P.n) {
-      if (P.scales) sv = P.scales[(size_t)r * P.ngroups + c / P.group];
-      if (P.cscales) sv = __fmul_rn(sv, P.cscales[c]);
-    }
-    se[j] = sv;
-    rcpe[j] = __frcp_rn(sv);
-  }
+  for (int j = 0; j < kPer; ++j) rcpe[j] = __frcp_rn(se[j]);
   const float flo = (float)P.lo, fhi = (float)P.hi;
   __syncthreads();
 #pragma unroll
