@@ -157,22 +157,28 @@ __device__ __forceinline__ float2 block_max2(float a, float b, unsigned* red) {
   return make_float2(__uint_as_float(ma), __uint_as_float(mb));
 }
 
-// Trailing update M[ib][jb] -= P[ib] C~[jb][kb]^T for kb < jb <= ib.
+// Trailing update M[ib][jb] -= P[ib] C~[jb][kb]^T for kb < jb <= ib, in
+// 64 x 64 tiles (2 x 2 blocks of NB): CTA (A, Bs) of the lower tile
+// triangle updates block rows kb+1+2A, kb+2+2A and block columns
+// kb+1+2Bs, kb+2+2Bs (entries with column <= row only).  Each thread holds
+// 16 outputs (rows ty + 8 rr, columns tx + 32 cc), so that every operand
+// value loaded from shared memory feeds 8 or 2 multiply-adds.
+constexpr int kTrail = 2 * NB;
 __global__ void __launch_bounds__(256) trailing_kernel(FParams F, int kb) {
-  __shared__ float2 sA[NB][NB + 1];  // P rows of block ib
-  __shared__ float2 sB[NB][NB + 1];  // C~ rows of block jb (panel kb)
+  __shared__ float2 sA[kTrail][NB + 1];  // P rows of the tile's two block rows
+  __shared__ float2 sB[kTrail][NB + 1];  // C~ rows of its two block columns (panel kb)
   __shared__ unsigned red[16];
   int a, b;
   tri_decode(blockIdx.x, a, b);
-  const int ib = kb + 1 + a, jb = kb + 1 + b;
+  const int r0 = (kb + 1 + 2 * a) * NB, c0 = (kb + 1 + 2 * b) * NB;  // first row, first column
   const int base = kb * NB;
   const int bs = min(NB, F.d - base);
   float amax = 0.f, bmax = 0.f;
-  for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
+  for (int e = threadIdx.x; e < kTrail * NB; e += blockDim.x) {
     const int u = e / NB, v = e % NB;
-    const int ra = ib * NB + u, rb = jb * NB + u;
-    float2 va = (ra < F.d && v < bs) ? F.P[(size_t)ra * NB + v] : make_float2(0.f, 0.f);
-    float2 vb = (rb < F.d && v < bs) ? F.M[(size_t)rb * F.d + base + v] : make_float2(0.f, 0.f);
+    const int ra = r0 + u, rb = c0 + u;
+    const float2 va = (ra < F.d && v < bs) ? F.P[(size_t)ra * NB + v] : make_float2(0.f, 0.f);
+    const float2 vb = (rb < F.d && v < bs) ? F.M[(size_t)rb * F.d + base + v] : make_float2(0.f, 0.f);
     sA[u][v] = va;
     sB[u][v] = vb;
     amax = fmaxf(amax, fabsf(va.x));
@@ -181,21 +187,32 @@ __global__ void __launch_bounds__(256) trailing_kernel(FParams F, int kb) {
   const float2 mx = block_max2(amax, bmax, red);
   const float sigma = offset_for_bound(2.f * NB * mx.x * mx.y);
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  OffsetAcc acc[4];
+  OffsetAcc acc[8][2];
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) acc[rr].init(sigma);
-  for (int t = 0; t < NB; ++t) {
-    const float2 bv = sB[tx][t];
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) acc[rr].mac(sA[ty + 8 * rr][t], bv);
+  for (int rr = 0; rr < 8; ++rr) {
+    acc[rr][0].init(sigma);
+    acc[rr][1].init(sigma);
   }
-  const int gc = jb * NB + tx;
+#pragma unroll 4
+  for (int t = 0; t < NB; ++t) {
+    const float2 b0 = sB[tx][t], b1 = sB[tx + NB][t];
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int gr = ib * NB + ty + 8 * rr;
-    if (gr < F.d && gc < F.d && gc <= gr) {
-      const size_t o = (size_t)gr * F.d + gc;
-      F.M[o] = df_sub(F.M[o], acc[rr].value(sigma));
+    for (int rr = 0; rr < 8; ++rr) {
+      const float2 av = sA[ty + 8 * rr][t];
+      acc[rr][0].mac(av, b0);
+      acc[rr][1].mac(av, b1);
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int gr = r0 + ty + 8 * rr;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int gc = c0 + tx + NB * cc;
+      if (gr < F.d && gc < F.d && gc <= gr) {
+        const size_t o = (size_t)gr * F.d + gc;
+        F.M[o] = df_sub(F.M[o], acc[rr][cc].value(sigma));
+      }
     }
   }
 }
@@ -321,8 +338,9 @@ cudaError_t factor_launch(const float* H, int d, float* Lhat, void* ws, int32_t*
     const int rows = d - std::min(d, (kb + 1) * NB);
     if (rows > 0) {
       panel_kernel<<<(rows + kPanelRows - 1) / kPanelRows, kPanelRows * NB, 0, stream>>>(F, kb);
-      const int nr = F.nb - kb - 1;
-      trailing_kernel<<<nr * (nr + 1) / 2, 256, 0, stream>>>(F, kb);
+      const int nr = F.nb - kb - 1;         // trailing block rows
+      const int nt = (nr + 1) / 2;          // 64-row tiles
+      trailing_kernel<<<nt * (nt + 1) / 2, 256, 0, stream>>>(F, kb);
     }
   }
   for (int b = NB; b < F.d; b *= 2) {
