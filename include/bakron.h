@@ -207,7 +207,10 @@ int bakron_gptq_quantize(const float* W, const float* LA, const float* scales, i
 size_t bakron_gram_workspace_size(int64_t d, int64_t N, int weighted);
 
 /* G <- beta G + alpha X diag(w) X^T on the tensor cores (tcgen05; every
- * bf16 product exact, fp32 accumulation over the samples).  A packing pass
+ * bf16 product exact; fp32 accumulation over segments of 2048 samples,
+ * whose sums are added in fp32, so the rounding error of an entry grows
+ * with the segment length and the number of segments, not with N: about
+ * 5e-6 relative, Frobenius norm, at 65536 samples).  A packing pass
  * rearranges X into `ws` first; the products then stream 16 KB blocks with
  * bulk copies.
  * X: device, bf16 bit patterns, d x ldx, 16-byte aligned, ldx >= N and a

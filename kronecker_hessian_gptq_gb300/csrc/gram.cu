@@ -42,8 +42,8 @@ namespace {
 constexpr int kGT = 128;                 // output tile edge (tensor-memory lanes, MMA N)
 constexpr int kGK = 64;                  // samples per stage: 8 groups of 8 (16 bytes)
 constexpr int kGStages = 3;
-constexpr int kGSegStages = 16;                 // stages per accumulation segment
-constexpr int kGSegSamples = kGSegStages * 64;  // 1024 samples
+constexpr int kGSegStages = 32;                 // stages per accumulation segment
+constexpr int kGSegSamples = kGSegStages * 64;  // 2048 samples
 constexpr int kGWarps = 8;
 constexpr int kGThreads = kGWarps * 32;
 constexpr uint32_t kGLbo = 128;              // stride of an 8-sample group within an 8-row block

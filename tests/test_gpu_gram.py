@@ -4,14 +4,16 @@ Kronecker-Factored Hessians", Sec. 4.2, App. A.2, App. D).
 
 Tolerance, from the arithmetic: every bf16 x bf16 product is exact in fp32;
 the tensor cores add the products of an entry in fp32 over segments of at
-most SEG = 1024 samples, and the kernel adds the nseg = ceil(N / SEG)
+most SEG = 2048 samples, and the kernel adds the nseg = ceil(N / SEG)
 segment sums into a running fp32 sum and scales it once by alpha.  So entry
 (i, j) is within (2 (min(N, SEG) + 16) + nseg) 2^-24 alpha sum_t
 |w_t x_it x_jt| of the exact value (the sequential fp32 summation bound of
 one segment, doubled for the order inside the MMA; one rounding per
 segment added and one for the scaling); with weights, the bf16 split of
 w_t x_t leaves 2^-16 relative per term more.  The typical error is also checked: Frobenius norm within
-1e-5 relative, at every N up to the 65536 samples of the full-size case."""
+1e-5 relative, at every N up to the 65536 samples of the full-size case,
+plus (with weights) the 2^-16 of alpha |X| diag(|w|) |X|^T the split may
+leave."""
 
 import numpy as np
 import pytest
@@ -22,7 +24,7 @@ from workloads.activations import make_sample_config, make_samples
 pytestmark = pytest.mark.gpu
 
 U = 2.0 ** -24
-SEG = 1024  # samples per fp32 accumulation segment of bakron_gram
+SEG = 2048  # samples per fp32 accumulation segment of bakron_gram
 
 
 @pytest.fixture(scope="module")
@@ -68,14 +70,23 @@ def _bound(Xf, w, alpha, weighted, rounded_weights=False):
     return S * rel + 1e-30
 
 
-def _check(G, ref, bound):
+def _split_norm(Xf, w, alpha):
+    """Frobenius norm of the error the bf16 split of w_t x_t may leave: 2^-16
+    (two roundings of 2^-17 at most) of alpha |X| diag(|w|) |X|^T."""
+    A = np.abs(Xf.astype(np.float64))
+    return 2.0 ** -16 * alpha * float(np.linalg.norm((A * np.abs(np.asarray(w, np.float64))[None, :]) @ A.T))
+
+
+def _check(G, ref, bound, frob_extra=0.0):
+    """Entrywise bound; Frobenius error within 1e-5 relative (plus, with
+    weights, what their bf16 split may leave)."""
     err = np.abs(G.astype(np.float64) - ref)
     assert np.all(err <= bound), float((err / bound).max())
-    assert np.linalg.norm(G - ref) <= 1e-5 * np.linalg.norm(ref) + 1e-30
+    assert np.linalg.norm(G - ref) <= 1e-5 * np.linalg.norm(ref) + frob_extra + 1e-30
     assert np.array_equal(G, G.T)
 
 
-@pytest.mark.parametrize("d,N", [(1, 1), (5, 7), (64, 64), (128, 100), (130, 1000), (257, 333), (64, 1100), (130, 3000)])
+@pytest.mark.parametrize("d,N", [(1, 1), (5, 7), (64, 64), (128, 100), (130, 1000), (257, 333), (64, 2100), (130, 5000)])
 @pytest.mark.parametrize("weighted", [False, True])
 def test_gram_against_oracle(bk, d, N, weighted):
     import torch
@@ -88,7 +99,8 @@ def test_gram_against_oracle(bk, d, N, weighted):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     ref = O.weighted_gram(Xf, w)
-    _check(G.cpu().numpy(), ref, _bound(Xf, w, 1.0 / N, weighted))
+    extra = _split_norm(Xf, w, 1.0 / N) if weighted else 0.0
+    _check(G.cpu().numpy(), ref, _bound(Xf, w, 1.0 / N, weighted), extra)
 
 
 def test_gram_accumulates_batches(bk):
@@ -119,8 +131,9 @@ def test_shampoo_one_step_end_to_end(bk):
     assert np.allclose(wa.cpu().numpy(), O.squared_norms(s.b_f32), rtol=1e-6, atol=0)
     Ao, Bo = O.shampoo_factors(s.a_f32, s.b_f32, 1)
     # the GPU's weights are the squared norms rounded once to fp32
-    _check(A.cpu().numpy(), Ao, _bound(s.a_f32, O.squared_norms(s.b_f32), 1 / 500, True, rounded_weights=True))
-    _check(B.cpu().numpy(), Bo, _bound(s.b_f32, O.squared_norms(s.a_f32), 1 / 500, True, rounded_weights=True))
+    wa_, wb_ = O.squared_norms(s.b_f32), O.squared_norms(s.a_f32)
+    _check(A.cpu().numpy(), Ao, _bound(s.a_f32, wa_, 1 / 500, True, rounded_weights=True), _split_norm(s.a_f32, wa_, 1 / 500))
+    _check(B.cpu().numpy(), Bo, _bound(s.b_f32, wb_, 1 / 500, True, rounded_weights=True), _split_norm(s.b_f32, wb_, 1 / 500))
 
 
 def test_damp_against_oracle(bk):
@@ -158,6 +171,7 @@ def test_gram_full_size_sampled_entries(bk):
     rel = np.linalg.norm(err) / np.linalg.norm(ref)
     worst = float((err / bnd).max())
     assert np.all(err <= bnd), (worst, rel)
-    # fp32 accumulation over 1024-sample segments, then 64 segment sums
+    # fp32 accumulation over 2048-sample segments, then 32 segment sums (measured 5.2e-6)
+    print(f"\ngram 4096 x 65536: Frobenius error {rel:.3g} relative, worst entry at {worst:.3g} of its bound")
     assert rel <= 1e-5, (worst, rel)
     assert np.array_equal(G, G.T)
