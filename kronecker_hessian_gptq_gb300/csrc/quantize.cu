@@ -622,17 +622,23 @@ struct TcStage {
 template <>
 struct TcStage<true> {};
 
+// Digit slab buffers: three with packed digits (bulk copies in flight while
+// two slabs wait for or feed the products), two when the producer warps
+// make them (their fp32 staging takes the room of the third).
+template <bool kPacked>
+constexpr int kDigBufs = kPacked ? 3 : 2;
+
 template <bool kPacked>
 struct TcSmem : TcStage<kPacked> {
-  __nv_bfloat16 A[2][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
+  __nv_bfloat16 A[kDigBufs<kPacked>][kDigF][kTcM * kSlab];  // factor digit slabs, core-matrix layout (SBO 512 B)
   __nv_bfloat16 Bd[kDigD * T * CK];         // source digits, 192 rows (digit-major) x CK, SBO 2048 B
   signed char er[kMaxItems][kTcM];          // row exponents of each item's factor block
   ChunkCand cand[kMaxItems];                // the candidate of each item
   int grp[kMaxItems];                       // its target group within the candidate
   int seg[kMaxItems];                       // 1 where an item starts a new candidate (after the first)
   int count;                                // items mapped (the CTA's share of the launch)
-  uint64_t full[2];                         // digit slab p ready (producer arrivals / bulk-copy bytes)
-  uint64_t empty[2];                        // products reading digit slab p done (commit)
+  uint64_t full[kDigBufs<kPacked>];         // digit slab p ready (producer arrivals / bulk-copy bytes)
+  uint64_t empty[kDigBufs<kPacked>];        // products reading digit slab p done (commit)
   uint64_t grp_full[2];                     // products of a group in tensor-memory half h done (commit)
   uint64_t grp_empty[2];                    // epilogue of tensor-memory half h done (epilogue arrivals)
   uint64_t bd_free;                         // products reading the source digits of a candidate done (commit)
@@ -693,6 +699,7 @@ template <bool kPacked>
 __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col, int ncand, int nitems,
                                                 int per_cand) {
   using Shape = TcShape<kPacked>;
+  constexpr int NBUF = kDigBufs<kPacked>;
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem<kPacked>& sm = *reinterpret_cast<TcSmem<kPacked>*>(tc_smem_raw);
   const int i0 = (int)(((long long)blockIdx.x * nitems) / gridDim.x);
@@ -804,10 +811,13 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col,
   }
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NBUF; ++i) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&sm.full[i])),
                    "r"(kPacked ? 1 : Shape::kProducers));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.empty[i])));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(&sm.grp_full[i])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;\n" ::"r"(smem_u32(&sm.grp_empty[i])));
     }
@@ -849,7 +859,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col,
       // lane 0.  The whole warp loads the next candidate's source digits.
       uint32_t nseg = 0;
       for (int z = 0; z < nz; ++z) {
-        const int p = z & 1, gi = z / nslab, s = z % nslab;
+        const int p = z % NBUF, gi = z / nslab, s = z % nslab;
         if (s == 0 && sm.seg[gi]) next_sources(gi, ++nseg, lane, 32);
         if (lane == 0) {
           const ChunkCand& cc = sm.cand[gi];
@@ -858,7 +868,7 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col,
           const int t0 = group_row0(gi) / T;
           const int ntg = min(UC, nt - t0);
           const uint32_t bytes = (uint32_t)ntg * 2048u;
-          if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+          if (z >= NBUF) mbar_wait(&sm.empty[p], (uint32_t)(z / NBUF - 1) & 1u, broken);
           if (!broken) {
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(&sm.full[p])),
                          "r"(bytes * kDigF)
@@ -882,10 +892,10 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col,
     } else {
       uint32_t nseg = 0;
       for (int z = 0; z < nz; ++z) {
-        const int p = z & 1, gi = z / nslab, s = z % nslab;
+        const int p = z % NBUF, gi = z / nslab, s = z % nslab;
         copy_slab(z + 2);
         asm volatile("cp.async.wait_group 2;\n" ::: "memory");  // this thread's items of slab z
-        if (z >= 2) mbar_wait(&sm.empty[p], (uint32_t)((z >> 1) - 1) & 1u, broken);
+        if (z >= NBUF) mbar_wait(&sm.empty[p], (uint32_t)(z / NBUF - 1) & 1u, broken);
         if (s == 0 && sm.seg[gi]) next_sources(gi, ++nseg, ptid, Shape::kProducers);
         for (int it = ptid; it < kTcM * kSlab / 8; it += Shape::kProducers) {
           const int r = it / 4, k8 = 8 * (it % 4);
@@ -920,10 +930,10 @@ __global__ void __maxnreg__(80) chunk_tc_kernel(QParams P, int K, int ncand_col,
     if (lane == 0) {
       uint32_t nseg = 0;
       for (int z = 0; z < nz; ++z) {
-        const int p = z & 1, gi = z / nslab, s = z % nslab, h = gi & 1;
+        const int p = z % NBUF, gi = z / nslab, s = z % nslab, h = gi & 1;
         if (s == 0 && gi >= 2) mbar_wait(&sm.grp_empty[h], (uint32_t)((gi >> 1) - 1) & 1u, broken);
         if (s == 0 && sm.seg[gi]) mbar_wait(&sm.bd_full, nseg++ & 1u, broken);
-        mbar_wait(&sm.full[p], (uint32_t)(z >> 1) & 1u, broken);
+        mbar_wait(&sm.full[p], (uint32_t)(z / NBUF) & 1u, broken);
         if (broken) break;
         tc_fence_after();
 #pragma unroll
