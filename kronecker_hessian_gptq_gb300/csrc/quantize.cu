@@ -655,10 +655,11 @@ struct TcSmem : TcStage<kPacked> {
 // row products, as their transpose:
 //   Gc[I, targets]^T += L_A[targets, chunk cols] E[I, chunk cols]^T.
 // Warp-specialized pipeline over the k-slabs of all items of the CTA:
-//  * the next slab's five factor digit blocks go into one of two digit
-//    buffers once the products that read that buffer are done: bulk copies
-//    of the packed digits by one thread, or fp32 slabs copied two ahead
-//    (cp.async) by the producer warps and split into digits there;
+//  * the next slab's five factor digit blocks go into one of the digit
+//    buffers (three with packed digits, else two) once the products that
+//    read that buffer are done: bulk copies of the packed digits by one
+//    thread, or fp32 slabs copied two ahead (cp.async) by the producer
+//    warps and split into digits there;
 //  * one thread issues, per 16-deep k-step, five MMAs: factor digit a times
 //    the source digits 0 .. 5-a stacked along N (N = 32 (6 - a)), written at
 //    tensor-memory column 32 a, so the block of source digit b lands on
@@ -1070,9 +1071,9 @@ class LaunchClock {
 // Calls that share a set serialize their side work on its streams, which
 // is correct: each call's main stream waits only on its own events' records.
 // Dynamic shared memory: a mid push CTA holds one stage; a chunk product
-// CTA the source digits, two factor digit slabs and, when it makes the
-// digits itself, three fp32 factor slabs (178 KB, else 130 KB: one per SM,
-// with room beside it for a tile solve).
+// CTA the source digits, three factor digit slabs with packed digits, or
+// two and three fp32 factor slabs when it makes the digits itself (about
+// 175 KB either way: one per SM, with room beside it for a tile solve).
 constexpr int kMidSmem = (int)sizeof(PushSmem<1>);
 template <bool kPacked>
 constexpr int kChunkSmem = (int)sizeof(TcSmem<kPacked>);
