@@ -1096,7 +1096,7 @@ constexpr int kChunkStreams = 1;
 struct StreamSet {
   bool ready = false;
   unsigned long long ctx_id = 0;  // context the streams and events belong to
-  cudaStream_t solve = nullptr, mid = nullptr, chunk[kChunkStreams] = {};
+  cudaStream_t solve = nullptr, mid = nullptr, mid_low = nullptr, chunk[kChunkStreams] = {};
   int sms = 0;  // multiprocessors of the device
   std::vector<cudaEvent_t> ev;
 };
@@ -1114,13 +1114,16 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     int lo = 0, hi = 0;
     e = cudaDeviceGetStreamPriorityRange(&lo, &hi);  // hi is the most urgent (numerically lowest)
     if (e != cudaSuccess) return e;
-    // Both side streams get the highest priority: the chunk products are
+    // The chunk stream gets the highest priority: the chunk products are
     // the largest block of work and their stream sets the pace (measured on
-    // c3: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms here).
-    (void)lo;
+    // c3: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms
+    // here).  The mid pushes run on a stream of either priority (see
+    // quantize_launch).
     e = cudaStreamCreateWithPriority(&S.solve, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return e;
     e = cudaStreamCreateWithPriority(&S.mid, cudaStreamNonBlocking, hi);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamCreateWithPriority(&S.mid_low, cudaStreamNonBlocking, lo);
     if (e != cudaSuccess) return e;
     for (int i = 0; i < kChunkStreams; ++i) {
       e = cudaStreamCreateWithPriority(&S.chunk[i], cudaStreamNonBlocking, hi);
@@ -1253,7 +1256,13 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   cudaEvent_t ev_start = ev_chunk[Kmax + 1];
   // With a timer every kernel runs on the caller's stream, one after the
   // other, so that each event pair brackets one kernel alone.
-  cudaStream_t s_mid = timer ? stream : S.mid;
+  // Mid pushes at the lowest priority from 2^22 weights on, so that the
+  // block scheduler places a pending tile solve's CTAs before theirs
+  // (measured on one GB300, 4096 x 4096: 13.6 against 14.0 ms, row-wise
+  // GPTQ 7.11 against 7.24 ms; 14336 x 4096 and 4096 x 14336 the same
+  // either way); at the highest on smaller layers, where they are on the
+  // chain's critical path (1024 x 1024: 2.35 against 2.41 ms).
+  cudaStream_t s_mid = timer ? stream : (use_packed_digits(m, n) ? S.mid_low : S.mid);
   // Layers up to 2^24 weights: the tile solves run on a stream of the
   // highest priority, beside the products (measured on 4096 x 4096: 15.9
   // against 16.6 ms); on larger layers the products set the pace, and the
@@ -1378,10 +1387,13 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
               P, K, ncc, ncc + ncr, nitems, kItemsPerCand);
       } else {
         // The launch's items shared evenly: small launches over at most
-        // three quarters of the SMs (one CTA each), so that the next tile
+        // five eighths of the SMs (one CTA each), so that the next tile
         // solves find SMs without a chunk product CTA; large ones in whole
         // waves of one CTA per SM; at most kMaxItems items per CTA.
-        const int cap = std::max(1, S.sms * 3 / 4);
+        // Measured on 4096 x 4096 (c3, mid pushes at the lowest priority):
+        // 13.51 ms at 5/8, 13.60 at 3/4, 13.77 at 7/8; 9/16 and 11/16 (with
+        // mid pushes at the highest priority) were between 5/8 and 3/4.
+        const int cap = std::max(1, S.sms * 5 / 8);
         int ctas = std::min(nitems, cap);
         if (nitems > cap * kMaxItems) {
           const int waves = (nitems + S.sms * kMaxItems - 1) / (S.sms * kMaxItems);
