@@ -1116,7 +1116,7 @@ cudaError_t prepare_set(StreamSet& S, size_t nev) {
     if (e != cudaSuccess) return e;
     // The chunk stream gets the highest priority: the chunk products are
     // the largest block of work and their stream sets the pace (measured on
-    // c3: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms
+    // 4096 x 4096: 23.3 ms with the chunk stream at the lowest priority, 22.6 ms
     // here).  The mid pushes run on a stream of either priority (see
     // quantize_launch).
     e = cudaStreamCreateWithPriority(&S.solve, cudaStreamNonBlocking, hi);
@@ -1390,7 +1390,7 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
         // five eighths of the SMs (one CTA each), so that the next tile
         // solves find SMs without a chunk product CTA; large ones in whole
         // waves of one CTA per SM; at most kMaxItems items per CTA.
-        // Measured on 4096 x 4096 (c3, mid pushes at the lowest priority):
+        // Measured on 4096 x 4096 (mid pushes at the lowest priority):
         // 13.51 ms at 5/8, 13.60 at 3/4, 13.77 at 7/8; 9/16 and 11/16 (with
         // mid pushes at the highest priority) were between 5/8 and 3/4.
         const int cap = std::max(1, S.sms * 5 / 8);
