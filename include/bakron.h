@@ -24,8 +24,10 @@
  *     a non-finite input) are written to a caller-provided device status
  *     word; nothing traps or asserts on the device.
  *   - Return values are bakron_status codes.
- *   - Process state: the solve keeps, per device, two side streams and a
- *     pool of ordering events (driver objects, not device memory), created
+ *   - Process state: the solve keeps, per device, four internal streams
+ *     (tile solves and chunk products at the highest priority, mid pushes
+ *     at the highest or the lowest) and a pool of ordering events (driver
+ *     objects, not device memory), created
  *     by the first call on the device; the no-allocation solve caches its
  *     scratch array's device address per device.  Both caches remember the
  *     CUDA context they were made in (cuCtxGetId) and are rebuilt when the
