@@ -51,8 +51,9 @@ extern "C" {
  * sweep is class 4); adds bakron_sweep_plan_check.
  * 4: bakron_quantize runs the tile wavefront on every device (measured
  * faster than the persistent sweep on every workload); the sweep is
- * bakron_quantize_persistent, and profile class 4 stays 0. */
-#define BAKRON_ABI_VERSION 4
+ * bakron_quantize_persistent, and profile class 4 stays 0.
+ * 5: adds bakron_wavefront_plan_check. */
+#define BAKRON_ABI_VERSION 5
 
 typedef enum bakron_status {
   BAKRON_OK = 0,
@@ -376,6 +377,26 @@ int bakron_quantize_host(const float* W, const float* LA, const float* LB, const
  * are none, BAKRON_ERR_INVALID_ARG for bad sizes, else 1.
  */
 int bakron_sweep_plan_check(int64_t m, int64_t n, int64_t* stats);
+
+/* Host-only check of bakron_quantize's launch schedule for an m x n layer
+ * (no GPU involved; the same step numbering, target ranges and chunk
+ * candidates as the launches): along every tile column (the column terms
+ * L_B[p, i] G[i, q], colpush = 1) and every tile row (the row terms
+ * E[p, j] L_A[q, j]) -- together the product L_B E L_A^T restricted to the
+ * later entries ("BaKron", App. B eq. (1)) -- each pair of a source tile and
+ * a later target tile is carried exactly once, by the target's own solve
+ * (adjacent tiles), a mid push or a chunk product; a mid push is complete
+ * two steps after its launch, a chunk product `lag` steps after (the solver
+ * waits B + 1 = 5 steps; other values test the check); every source is
+ * solved before its push is launched and every tile is solved once.
+ * colpush = 0 checks the row-wise schedule of bakron_gptq_quantize (L_B = I:
+ * no column terms, tile columns as steps).  m, n in 1 .. 2^15.
+ * stats (host, 3 entries): [0] pulls and pushes recorded, [1] the smallest
+ * number of steps from a chunk product's launch to its first target's solve
+ * (-1 without chunk products), [2] errors.  Returns BAKRON_OK when there are
+ * none, BAKRON_ERR_INVALID_ARG for bad arguments, else 1.
+ */
+int bakron_wavefront_plan_check(int64_t m, int64_t n, int colpush, int lag, int64_t* stats);
 
 /* --------------------------------------------------------------- self-test
  * Exercises the device-side timeout path on purpose: one thread waits, with

@@ -61,6 +61,7 @@ SIGNATURES = {
     "bakron_quantize_host": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
     "bakron_quantize_noalloc": (_int, [_vp, _vp, _vp, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp]),
     "bakron_sweep_plan_check": (_int, [_i64, _i64, _vp]),
+    "bakron_wavefront_plan_check": (_int, [_i64, _i64, _int, _int, _vp]),
 }
 
 _lib = None

@@ -256,6 +256,12 @@ int bakron_sweep_plan_check(int64_t m, int64_t n, int64_t* stats) {
   return bakron::sweep_plan_check(m, n, stats) == 0 ? BAKRON_OK : 1;
 }
 
+int bakron_wavefront_plan_check(int64_t m, int64_t n, int colpush, int lag, int64_t* stats) {
+  if (!stats || m < 1 || n < 1 || m > (int64_t)1 << 15 || n > (int64_t)1 << 15 || lag < 1 || (colpush != 0 && colpush != 1))
+    return BAKRON_ERR_INVALID_ARG;
+  return bakron::wavefront_plan_check(m, n, colpush != 0, lag, stats) == 0 ? BAKRON_OK : 1;
+}
+
 int bakron_quantize_profile(const float* W, const float* LA, const float* LB, const float* scales, int bits,
                             int64_t m, int64_t n, int32_t* V, float* Wq, void* ws, size_t ws_bytes,
                             int32_t* status_dev, void* stream, double* kernel_ms, int64_t* kernel_launches,

@@ -56,6 +56,8 @@ size_t quantize_workspace_bytes(int64_t m, int64_t n);
 cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Scales sc,
                             Alphabet al, int m, int n, int32_t* V, float* Wq, void* ws,
                             int32_t* status_dev, cudaStream_t stream, KernelTimer* timer = nullptr);
+// Host-only check of quantize_launch's schedule (see quantize.cu).
+int wavefront_plan_check(int64_t m, int64_t n, bool colpush, int lag, int64_t* stats);
 
 // sweep.cu (the persistent band sweep: one cooperative kernel per solve)
 size_t sweep_workspace_bytes(int64_t m, int64_t n);

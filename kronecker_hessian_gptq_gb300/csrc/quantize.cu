@@ -556,7 +556,8 @@ struct ChunkCand {
   bool col;
   int J, I, c, first, ntiles;
 };
-__device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int ncand_col, int t, ChunkCand& cc) {
+__host__ __device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int ncand_col, int t,
+                                                         ChunkCand& cc) {
   cc.col = t < ncand_col;
   if (cc.col) {
     cc.J = K - (B - 1) - B * t;
@@ -585,6 +586,14 @@ __device__ __forceinline__ bool chunk_candidate(const QParams& P, int K, int nca
     cc.ntiles = P.Nt - cc.first;
   }
   return cc.ntiles > 0;
+}
+
+// Candidates of the chunk products closed by step K (chunk_candidate's t
+// ranges over ncc column candidates, then ncr row candidates).
+inline void chunk_counts(const QParams& P, int K, bool colpush, int& ncc, int& ncr) {
+  ncc = (colpush && std::min(K, P.Mt - 1) >= B - 1) ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
+  ncr = P.skew ? (std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0)
+               : ((K + 1) % B == 0 ? P.Mt : 0);  // tile columns: every row closes a chunk
 }
 
 // Warp roles of a chunk product CTA.
@@ -1348,30 +1357,17 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
       last_mid = K;
     }
 
-    // chunk products closed by K
-    const int ncc = (LB && std::min(K, P.Mt - 1) >= B - 1) ? (std::min(K, P.Mt - 1) - (B - 1)) / B + 1 : 0;
-    const int ncr = P.skew ? (std::min(K, P.Nt - 1) >= B - 1 ? (std::min(K, P.Nt - 1) - (B - 1)) / B + 1 : 0)
-                           : ((K + 1) % B == 0 ? P.Mt : 0);  // tile columns: every row closes a chunk
-    // The same candidates as chunk_candidate, and their items (target groups).
+    // chunk products closed by K, and their items (target groups)
+    int ncc = 0, ncr = 0;
+    chunk_counts(P, K, LB != nullptr, ncc, ncr);
     double chunk_tiles = 0;
     int nitems = 0, most = 0;  // items (target groups) in all; most of one candidate
-    for (int t = 0; t < ncc; ++t) {
-      const int J = K - (B - 1) - B * t, last = K - J;
-      if (J >= 0 && J < P.Nt && last < P.Mt) {
-        const int nt = std::max(0, P.Mt - (last / B + 2) * B);
-        chunk_tiles += nt;
-        nitems += (nt + UC - 1) / UC;
-        most = std::max(most, (nt + UC - 1) / UC);
-      }
-    }
-    for (int t = 0; t < ncr; ++t) {
-      const int I = P.skew ? K - (B - 1) - B * t : t, last = K - P.skew * I;
-      if (I >= 0 && I < P.Mt && last < P.Nt) {
-        const int nt = std::max(0, P.Nt - (last / B + 2) * B);
-        chunk_tiles += nt;
-        nitems += (nt + UC - 1) / UC;
-        most = std::max(most, (nt + UC - 1) / UC);
-      }
+    for (int t = 0; t < ncc + ncr; ++t) {
+      ChunkCand cc;
+      if (!chunk_candidate(P, K, ncc, t, cc)) continue;
+      chunk_tiles += cc.ntiles;
+      nitems += (cc.ntiles + UC - 1) / UC;
+      most = std::max(most, (cc.ntiles + UC - 1) / UC);
     }
     if (chunk_tiles > 0) {
       cudaStreamWaitEvent(s_chunk(K), ev_solve[K], 0);
@@ -1420,6 +1416,122 @@ cudaError_t quantize_launch(const float* W, const float* LA, const float* LB, Sc
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   return clock.finish(stream);
+}
+
+// Host-only check of the launch schedule above, from the same pieces
+// (step numbering, mid_end and mid_push_kernel's target ranges,
+// chunk_counts and chunk_candidate).  Along every tile column (column
+// terms, when L_B is given) and every tile row (row terms), each pair of a
+// source tile s and a later target tile t must be carried exactly once: by
+// the target's own solve (t = s + 1, the distance-1 pulls), by a mid push
+// or by a chunk product.  A mid push launched after step K reaches its
+// targets when the solve of step K + 2 waits for it; a chunk product when
+// the solve of step K + lag does (quantize_launch: lag = B + 1); the mid
+// and chunk streams each run their launches in order.  Every source must be
+// solved by the step after which its push is launched, every tile solved
+// exactly once, and mid_push_kernel's grid must reach every target group.
+// stats: [0] pushes and pulls recorded, [1] the smallest number of steps
+// between a chunk product's launch and its first target's solve (-1 if
+// there is none), [2] errors.  Returns 0 when there are none.
+int wavefront_plan_check(int64_t m, int64_t n, bool colpush, int lag, int64_t* stats) {
+  QParams P{};
+  P.Mt = (int)((m + T - 1) / T);
+  P.Nt = (int)((n + T - 1) / T);
+  P.skew = colpush ? 1 : 0;
+  const int Kmax = P.skew ? P.Mt + P.Nt - 2 : P.Nt - 1;
+  auto step_of = [&](int I, int J) { return J + P.skew * I; };
+  struct Rec {
+    bool col;  // column terms (line = tile column J, indices = tile rows), else row terms
+    int line, s0, s1, t0, t1, K, kind;  // kind 0: pull, 1: mid push, 2: chunk product
+  };
+  std::vector<Rec> recs;
+  int64_t errors = 0;
+  std::vector<int> solved((size_t)P.Mt * P.Nt, -1);
+  const int units = 2 * ((2 * B - 2 + U - 1) / U);  // mid_push_kernel's grid.y
+  for (int K = 0; K <= Kmax; ++K) {
+    const int I0 = P.skew ? std::max(0, K - (P.Nt - 1)) : 0;
+    const int I1 = P.skew ? std::min(K, P.Mt - 1) : P.Mt - 1;
+    for (int I = I0; I <= I1; ++I) {
+      const int J = K - P.skew * I;
+      if (J < 0 || J >= P.Nt) {
+        ++errors;
+        continue;
+      }
+      if (solved[(size_t)I * P.Nt + J] >= 0) ++errors;
+      solved[(size_t)I * P.Nt + J] = K;
+      if (colpush && I > 0) recs.push_back({true, J, I - 1, I, I, I + 1, K, 0});
+      if (J > 0) recs.push_back({false, I, J - 1, J, J, J + 1, K, 0});
+      const int c_first = I + 2, c_end = colpush ? std::min(P.Mt, mid_end(I)) : c_first;
+      const int r_first = J + 2, r_end = std::min(P.Nt, mid_end(J));
+      const int ncu = c_end > c_first ? (c_end - c_first + U - 1) / U : 0;
+      const int nru = r_end > r_first ? (r_end - r_first + U - 1) / U : 0;
+      if (ncu + nru > units) ++errors;
+      if (c_end > c_first) recs.push_back({true, J, I, I + 1, c_first, c_end, K, 1});
+      if (r_end > r_first) recs.push_back({false, I, J, J + 1, r_first, r_end, K, 1});
+    }
+    int ncc = 0, ncr = 0;
+    chunk_counts(P, K, colpush, ncc, ncr);
+    for (int t = 0; t < ncc + ncr; ++t) {
+      ChunkCand cc;
+      if (!chunk_candidate(P, K, ncc, t, cc)) continue;
+      const int len = cc.col ? P.Mt : P.Nt;
+      recs.push_back({cc.col, cc.col ? cc.J : cc.I, cc.c * B, std::min((cc.c + 1) * B, len), cc.first,
+                      cc.first + cc.ntiles, K, 2});
+    }
+  }
+  for (int v : solved)
+    if (v < 0) ++errors;
+  int64_t min_slack = -1;
+  for (int dir = 0; dir < 2; ++dir) {
+    const bool col = dir == 0;
+    if (col && !colpush) {
+      for (const Rec& r : recs)
+        if (r.col) ++errors;
+      continue;
+    }
+    const int nlines = col ? P.Nt : P.Mt, len = col ? P.Mt : P.Nt;
+    std::vector<std::vector<const Rec*>> by_line(nlines);
+    for (const Rec& r : recs)
+      if (r.col == col) {
+        if (r.line < 0 || r.line >= nlines) {
+          ++errors;
+          continue;
+        }
+        by_line[r.line].push_back(&r);
+      }
+    std::vector<int> cnt((size_t)len * len);
+    for (int line = 0; line < nlines; ++line) {
+      std::fill(cnt.begin(), cnt.end(), 0);
+      for (const Rec* r : by_line[line]) {
+        if (r->s0 < 0 || r->s1 > len || r->t0 < 0 || r->t1 > len) {
+          ++errors;
+          continue;
+        }
+        for (int s = r->s0; s < r->s1; ++s) {
+          const int src_step = col ? step_of(s, line) : step_of(line, s);
+          if (r->kind == 0 ? src_step >= r->K : src_step > r->K) ++errors;  // source not solved in time
+          for (int t = r->t0; t < r->t1; ++t) {
+            if (t <= s) {
+              ++errors;
+              continue;
+            }
+            ++cnt[(size_t)s * len + t];
+            const int tgt_step = col ? step_of(t, line) : step_of(line, t);
+            const int need = r->kind == 0 ? 0 : (r->kind == 1 ? 2 : lag);
+            if (r->kind == 0 ? tgt_step != r->K : tgt_step < r->K + need) ++errors;
+            if (r->kind == 2 && (min_slack < 0 || tgt_step - r->K < min_slack)) min_slack = tgt_step - r->K;
+          }
+        }
+      }
+      for (int s = 0; s < len; ++s)
+        for (int t = s + 1; t < len; ++t)
+          if (cnt[(size_t)s * len + t] != 1) ++errors;
+    }
+  }
+  stats[0] = (int64_t)recs.size();
+  stats[1] = min_slack;
+  stats[2] = errors;
+  return errors == 0 ? 0 : 1;
 }
 
 }  // namespace bakron

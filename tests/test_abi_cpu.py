@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
                  "bakron_status_string", "bakron_abi_version", "bakron_gptq_quantize",
                  "bakron_antidiag_quantize", "bakron_quantize_range", "bakron_quantize_scaled",
                  "bakron_row_scales", "bakron_pack_codes", "bakron_gram", "bakron_sq_norms", "bakron_damp",
-                 "bakron_selftest_wait_timeout", "bakron_quantize_noalloc", "bakron_quantize_persistent"):
+                 "bakron_selftest_wait_timeout", "bakron_quantize_noalloc", "bakron_quantize_persistent",
+                 "bakron_wavefront_plan_check"):
         assert need in names
 
 
@@ -47,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.bakron_abi_version() == 4
+    assert lib.bakron_abi_version() == 5
     assert lib.bakron_status_string(0) == b"BAKRON_OK"
     assert lib.bakron_status_string(4) == b"BAKRON_ERR_WORKSPACE"
     assert lib.bakron_status_string(99) == b"BAKRON_ERR_UNKNOWN"
